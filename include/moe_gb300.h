@@ -1,0 +1,169 @@
+/*
+ * moe_gb300.h -- C ABI of the routed Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * One layer: T tokens of hidden size H are scored by a router against E experts,
+ * each token is sent to its top-k experts, every expert is a SwiGLU MLP whose
+ * three matrices are stored in NVFP4, and the k expert outputs of each token are
+ * weighted and summed. Sources (web pages on serving Kimi-K3):
+ *   - "Kimi-K3 NVFP4 station eight sparks", section "The number the project hangs
+ *     on": a layer is attention, then a router, then 16 experts, then a sum;
+ *     table "What we verified today": 16 of 896 experts per token, one expert is
+ *     18,579,480 bytes in 12 tensors; section "What has to be built": NVFP4 is an
+ *     FP8 scale per 16 values plus a per-expert global scale.
+ *   - "Serving Kimi-K3 ... with 8xB300 GPUs", section "The model, as the serving
+ *     system sees it": 3 matrices per expert, 4-bit E2M1 values two per byte.
+ *   - SemiAnalysis essay on MoE serving (Chinese translation), sections 4 and 15:
+ *     route records are sorted by expert so one weight load serves a bucket, then
+ *     expert outputs are restored to token order, weighted and merged.
+ * The pages leave open the score function, tie rule, activation and global-scale
+ * granularity; this library uses: fp32 router logits; top-k by (logit descending,
+ * expert index ascending, -0 == +0); gate weights = softmax over the k selected
+ * logits; SwiGLU silu(gate) * up with gate rows first; one fp32 scale per
+ * projection tensor (gate, up, down) per expert.
+ *
+ * Conventions for every call:
+ *   - Return value: MOE_OK (0) or a negative moe_status. Argument errors are
+ *     detected on the host before any GPU work is enqueued; nothing is written.
+ *   - "device" pointers are CUDA global memory on the context's device; "host"
+ *     pointers are CPU memory. Streams are passed as void* and must be a
+ *     cudaStream_t of the context's device (NULL = legacy default stream).
+ *   - Kernels never trap. Device-side anomalies (an expert id out of range, a
+ *     count overflow) set a sticky error word read by moe_get_error().
+ *   - A context is used by one host thread and one stream at a time.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx; /* opaque; owned by the library */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, T out of range, aliasing */
+  MOE_ERR_UNSUPPORTED = -2,  /* shape outside the supported set, or device is not sm_103 */
+  MOE_ERR_NOT_LOADED = -3,   /* forward before moe_load_layer */
+  MOE_ERR_OOM = -4,          /* device allocation failed */
+  MOE_ERR_CUDA = -5,         /* a CUDA runtime call failed */
+  MOE_ERR_DEVICE_FLAG = -6   /* a kernel raised the device error word */
+} moe_status;
+
+/* Layer shape and capacity.
+ * Supported: hidden % 256 == 0, inter % 128 == 0, 1 <= top_k <= 32,
+ * top_k <= n_experts <= 1024, 1 <= max_tokens, max_tokens * top_k < 2^31,
+ * hidden <= 14336. */
+typedef struct {
+  int32_t hidden;     /* H */
+  int32_t inter;      /* I, the expert intermediate size */
+  int32_t n_experts;  /* E */
+  int32_t top_k;      /* k */
+  int32_t max_tokens; /* the largest T a forward call may pass; sizes the workspace */
+  uint32_t flags;     /* reserved, must be 0 */
+} moe_config;
+
+/* One layer's weights in HOST memory, caller-owned, read only during moe_load_layer.
+ * Per-expert pointers let a caller hand over experts wherever they sit (a loader
+ * must map expert ids to tensors explicitly; checkpoints may store them out of order).
+ *   router_w    fp32 [H][E], row-major: logit[t][e] = sum_h x[t][h] * router_w[h][e]
+ *   router_bias fp32 [E] added to the logits, or NULL for none
+ *   gu_codes[e] uint8 [2I][H/2]: rows 0..I-1 gate, I..2I-1 up; element k of a row is
+ *               in byte k/2, low nibble = even k; a nibble is an E2M1 code
+ *   gu_scales[e] uint8 [2I][H/16]: E4M3 ("fn") scale of elements 16b..16b+15 of a row
+ *   gu_global   fp32 [E][2]: (gate, up) tensor scales
+ *   dn_codes[e] uint8 [H][I/2], dn_scales[e] uint8 [H][I/16], dn_global fp32 [E]
+ * Weight element = e2m1(code) * e4m3(block scale) * tensor scale. */
+typedef struct {
+  const float* router_w;
+  const float* router_bias;
+  const uint8_t* const* gu_codes;
+  const uint8_t* const* gu_scales;
+  const float* gu_global;
+  const uint8_t* const* dn_codes;
+  const uint8_t* const* dn_scales;
+  const float* dn_global;
+} moe_layer_host;
+
+/* Create a context on CUDA device `device`: checks the device is sm_103 and
+ * allocates the device workspace for cfg->max_tokens. *out receives the context
+ * (NULL on failure). */
+MOE_API int moe_create(const moe_config* cfg, int device, moe_ctx** out);
+
+/* Copy a layer's weights to the device and repack them into the kernels' layouts.
+ * Synchronous. May be called again to replace the layer. */
+MOE_API int moe_load_layer(moe_ctx* ctx, const moe_layer_host* layer);
+
+/* The layer on T tokens: out[t][:] = sum_j w[t][j] * FFN_{idx[t][j]}(x[t][:]).
+ *   x    device bf16 [T][H], row-major, 16-byte aligned
+ *   out  device bf16 [T][H], 16-byte aligned, must not overlap x
+ * Asynchronous on `stream`; allocates nothing; does not synchronise the host.
+ * T == 0 returns MOE_OK and enqueues nothing; T > max_tokens is an error. */
+MOE_API int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T);
+
+/* The same through HOST buffers: copies x (host bf16 [T][H]) to the device,
+ * runs moe_forward, copies the result to out (host bf16 [T][H]) and waits for
+ * the stream. Use page-locked host memory for asynchronous copies. */
+MOE_API int moe_forward_host(moe_ctx* ctx, void* stream, const void* x_host, void* out_host, int32_t T);
+
+/* Release everything the context owns. NULL is a no-op. */
+MOE_API int moe_destroy(moe_ctx* ctx);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_str(int status);
+
+/* Read and clear the device error word (synchronises the device). Returns
+ * MOE_OK if no kernel raised it, MOE_ERR_DEVICE_FLAG otherwise; *bits (may be
+ * NULL) receives the raw word: 1 = expert id out of range, 2 = row count overflow. */
+MOE_API int moe_get_error(moe_ctx* ctx, uint32_t* bits);
+
+/* ---- inspection hooks (tests and benchmarking) ----------------------------- */
+
+/* Routing of T tokens (router, select, permute). Every output is a device
+ * pointer and may be NULL:
+ *   logits fp32 [T][E]; idx int32 [T][k] (descending logit); w fp32 [T][k];
+ *   offsets int32 [E+1]; perm int32 [T*k] (token of routed row p);
+ *   slot int32 [T*k] (j of routed row p); inv int32 [T*k] (row p of (t, j)). */
+MOE_API int moe_debug_route(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* logits, int32_t* idx, float* w,
+                    int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv);
+
+/* Select and permute from caller-given logits (device fp32 [T][E]); the
+ * outputs are as for moe_debug_route. */
+MOE_API int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, int32_t T, int32_t* idx, float* w,
+                     int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv);
+
+/* The expert stage on its own: runs the whole layer on x and copies the SwiGLU
+ * activations h (device fp32 [T*k][I], rows in routed order p) and the
+ * unweighted down projections y (device fp32 [T*k][H]) out. Either may be NULL. */
+MOE_API int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y);
+
+/* Per-kernel timing with CUDA events recorded on the forward's stream.
+ * moe_profile_begin arms the next `max_calls` forwards; moe_profile_end waits
+ * for them and writes, for each of `n` stages (n <= moe_profile_stages()), the
+ * summed milliseconds and the number of launches timed. Stage names come from
+ * moe_profile_stage_name(i). */
+MOE_API int moe_profile_stages(void);
+MOE_API const char* moe_profile_stage_name(int i);
+MOE_API int moe_profile_begin(moe_ctx* ctx, int32_t max_calls);
+MOE_API int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n);
+
+/* Number of kernels this context has enqueued so far (all calls that run kernels). */
+MOE_API int64_t moe_launch_count(const moe_ctx* ctx);
+
+/* Device bytes held by the context (weights + workspace). */
+MOE_API int64_t moe_device_bytes(const moe_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,252 @@
+"""routed_expert_layer_gb300 -- a routed Mixture-of-Experts layer for GB300 (sm_103a).
+
+Thin Python binding over the C ABI declared in ``include/moe_gb300.h``: argument
+marshalling only. Every step of the layer runs in the library's CUDA kernels;
+PyTorch is used by callers for device memory and streams. There is no CPU path:
+if the CUDA library is missing, importing ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_BUILD = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_BUILD, "libmoe_gb300.so")
+_SOURCES = ["api.cu", "route.cu", "expert_simt.cu"]
+_HEADERS = ["moe_internal.cuh"]
+NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+              "--expt-relaxed-constexpr"]
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_NOT_LOADED = 0, -1, -2, -3
+MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_DEVICE_FLAG = -4, -5, -6
+
+EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "moe_destroy", "moe_status_str",
+            "moe_get_error", "moe_debug_route", "moe_debug_select", "moe_debug_experts", "moe_profile_stages",
+            "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count"]
+
+# Revision of each kernel's code; a stored ncu traffic figure is only reported while
+# the revision it was measured on is current.
+KERNEL_REV = {"router": "simt-1", "select": "warp-1", "permute": "mask-1", "gateup": "simt-1", "down": "simt-1",
+              "combine": "f32-1"}
+
+
+def _nvcc() -> str:
+    for p in ("/usr/local/cuda/bin/nvcc",):
+        if os.path.exists(p):
+            return p
+    return "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library in-tree for sm_103a (one -gencode, parallel TUs)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    deps = [os.path.join(_CSRC, f) for f in _SOURCES + _HEADERS] + [os.path.join(_ROOT, "include", "moe_gb300.h")]
+    newest = max(os.path.getmtime(d) for d in deps)
+    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
+        return LIB_PATH
+    nvcc = _nvcc()
+
+    def compile_one(src):
+        obj = os.path.join(_BUILD, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *NVCC_ARCH, *NVCC_FLAGS, "-c", os.path.join(_CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+        if verbose and r.stderr:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, _SOURCES))
+    tmp = LIB_PATH + ".tmp"
+    r = subprocess.run([nvcc, *NVCC_ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class LayerHost(ctypes.Structure):
+    _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("gu_codes", ctypes.POINTER(ctypes.c_void_p)), ("gu_scales", ctypes.POINTER(ctypes.c_void_p)),
+                ("gu_global", ctypes.c_void_p),
+                ("dn_codes", ctypes.POINTER(ctypes.c_void_p)), ("dn_scales", ctypes.POINTER(ctypes.c_void_p)),
+                ("dn_global", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded C library. Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        p, i32, vp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+        L.moe_create.argtypes = [ctypes.POINTER(Config), ctypes.c_int, ctypes.POINTER(vp)]
+        L.moe_load_layer.argtypes = [vp, ctypes.POINTER(LayerHost)]
+        L.moe_forward.argtypes = [vp, vp, p, p, i32]
+        L.moe_forward_host.argtypes = [vp, vp, p, p, i32]
+        L.moe_destroy.argtypes = [vp]
+        L.moe_status_str.restype = ctypes.c_char_p
+        L.moe_status_str.argtypes = [ctypes.c_int]
+        L.moe_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.moe_debug_route.argtypes = [vp, vp, p, i32, p, p, p, p, p, p, p]
+        L.moe_debug_select.argtypes = [vp, vp, p, i32, p, p, p, p, p, p]
+        L.moe_debug_experts.argtypes = [vp, vp, p, i32, p, p]
+        L.moe_profile_stage_name.restype = ctypes.c_char_p
+        L.moe_profile_stage_name.argtypes = [ctypes.c_int]
+        L.moe_profile_begin.argtypes = [vp, i32]
+        L.moe_profile_end.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32), i32]
+        L.moe_device_bytes.restype = ctypes.c_int64
+        L.moe_device_bytes.argtypes = [vp]
+        L.moe_launch_count.restype = ctypes.c_int64
+        L.moe_launch_count.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {lib().moe_status_str(status).decode()} ({status})")
+        self.status = status
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _dptr(t):
+    """Device pointer of a torch tensor (or None)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class MoeLayer:
+    """One routed expert layer on one GPU (wraps a moe_ctx)."""
+
+    def __init__(self, hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, device: int = 0):
+        self.cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0)
+        self.device = device
+        self.ctx = ctypes.c_void_p()
+        _check(lib().moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self.ctx)), "moe_create")
+
+    @property
+    def H(self):
+        return self.cfg.hidden
+
+    @property
+    def k(self):
+        return self.cfg.top_k
+
+    def load(self, layer) -> None:
+        """layer: object with numpy arrays gu_codes [E][2I][H/2], gu_scales, gu_global [E][2],
+        dn_codes [E][H][I/2], dn_scales, dn_global [E], router_w [H][E], router_bias [E] or None."""
+        E = self.cfg.n_experts
+        keep = []
+
+        def arr(a, dtype):
+            a = np.ascontiguousarray(a, dtype=dtype)
+            keep.append(a)
+            return a
+
+        def per_expert(a):
+            a = arr(a, np.uint8)
+            assert a.shape[0] == E
+            ptrs = (ctypes.c_void_p * E)(*[a.ctypes.data + e * a.strides[0] for e in range(E)])
+            keep.append(ptrs)
+            return ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+
+        rw = arr(layer.router_w, np.float32)
+        rb = None if layer.router_bias is None else arr(layer.router_bias, np.float32)
+        lh = LayerHost(rw.ctypes.data, None if rb is None else rb.ctypes.data,
+                       per_expert(layer.gu_codes), per_expert(layer.gu_scales),
+                       arr(layer.gu_global, np.float32).ctypes.data,
+                       per_expert(layer.dn_codes), per_expert(layer.dn_scales),
+                       arr(layer.dn_global, np.float32).ctypes.data)
+        _check(lib().moe_load_layer(self.ctx, ctypes.byref(lh)), "moe_load_layer")
+
+    def forward(self, x, out, stream=None) -> None:
+        """x, out: CUDA tensors of bf16 [T][H] (any dtype with 2-byte elements)."""
+        T = x.shape[0]
+        _check(lib().moe_forward(self.ctx, _stream(stream), _dptr(x), _dptr(out), T), "moe_forward")
+
+    def forward_host(self, x_host, out_host, stream=None) -> None:
+        """x_host, out_host: host buffers (numpy uint16 or pinned torch tensors) of [T][H] bf16."""
+        T = x_host.shape[0]
+        xp = x_host.ctypes.data if isinstance(x_host, np.ndarray) else x_host.data_ptr()
+        op = out_host.ctypes.data if isinstance(out_host, np.ndarray) else out_host.data_ptr()
+        _check(lib().moe_forward_host(self.ctx, _stream(stream), ctypes.c_void_p(xp), ctypes.c_void_p(op), T),
+               "moe_forward_host")
+
+    def debug_route(self, x, logits=None, idx=None, w=None, offsets=None, perm=None, slot=None, inv=None,
+                    stream=None):
+        _check(lib().moe_debug_route(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(logits), _dptr(idx),
+                                     _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
+               "moe_debug_route")
+
+    def debug_select(self, logits, idx=None, w=None, offsets=None, perm=None, slot=None, inv=None, stream=None):
+        _check(lib().moe_debug_select(self.ctx, _stream(stream), _dptr(logits), logits.shape[0], _dptr(idx),
+                                      _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
+               "moe_debug_select")
+
+    def debug_experts(self, x, h=None, y=None, stream=None):
+        _check(lib().moe_debug_experts(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(h), _dptr(y)),
+               "moe_debug_experts")
+
+    def get_error(self) -> int:
+        bits = ctypes.c_uint32(0)
+        st = lib().moe_get_error(self.ctx, ctypes.byref(bits))
+        if st not in (MOE_OK, MOE_ERR_DEVICE_FLAG):
+            _check(st, "moe_get_error")
+        return bits.value
+
+    def profile_begin(self, max_calls: int) -> None:
+        _check(lib().moe_profile_begin(self.ctx, max_calls), "moe_profile_begin")
+
+    def profile_end(self) -> dict:
+        n = lib().moe_profile_stages()
+        ms = (ctypes.c_float * n)()
+        cnt = (ctypes.c_int32 * n)()
+        _check(lib().moe_profile_end(self.ctx, ms, cnt, n), "moe_profile_end")
+        return {lib().moe_profile_stage_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
+
+    def launch_count(self) -> int:
+        """Kernels this layer has enqueued so far."""
+        return lib().moe_launch_count(self.ctx)
+
+    def device_bytes(self) -> int:
+        return lib().moe_device_bytes(self.ctx)
+
+    def close(self) -> None:
+        if self.ctx:
+            lib().moe_destroy(self.ctx)
+            self.ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

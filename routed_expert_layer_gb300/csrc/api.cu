@@ -1,0 +1,448 @@
+// C ABI: context, weight loading, the forward launch sequence, inspection hooks.
+// The operations and their sources are documented in include/moe_gb300.h.
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_ctx {
+  moe_config cfg{};
+  Shape sh{};
+  int device = 0;
+  int sm_count = 0;
+  bool loaded = false;
+  DeviceLayer L{};
+  Workspace ws{};
+  void* weights_mem = nullptr;
+  size_t weights_bytes = 0;
+  void* ws_mem = nullptr;
+  size_t ws_bytes = 0;
+  int64_t launches = 0;  // kernels enqueued by forward calls
+  // profiling
+  int prof_max = 0;
+  int prof_calls = 0;
+  std::vector<cudaEvent_t> prof_ev;  // [prof_max][kNumStages][2]
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+const char* kStageNames[kNumStages] = {"router", "select", "permute", "gateup", "down", "combine"};
+
+int check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->flags != 0) return MOE_ERR_INVALID_ARG;
+  if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->hidden % 256 != 0 || c->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->hidden > 14336) return MOE_ERR_UNSUPPORTED;
+  if (c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->max_tokens * c->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Carve `bytes` from a bump allocator (256-byte aligned).
+template <typename T>
+T* carve(char*& cur, size_t count) {
+  T* p = reinterpret_cast<T*>(cur);
+  size_t bytes = (count * sizeof(T) + 255) & ~(size_t)255;
+  cur += bytes;
+  return p;
+}
+
+size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* base) {
+  const size_t T = c.max_tokens, E = c.n_experts, k = c.top_k, H = c.hidden, I = c.inter;
+  const size_t C = (T + 31) / 32;
+  Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
+  char* cur = base;
+  Workspace w;
+  w.router_part = carve<float>(cur, router_part_elems(sh, c.max_tokens, sm_count));
+  w.logits = carve<float>(cur, T * E);
+  w.idx = carve<int32_t>(cur, T * k);
+  w.w = carve<float>(cur, T * k);
+  w.masks = carve<uint32_t>(cur, C * E);
+  w.chunk_base = carve<int32_t>(cur, C * E);
+  w.counts = carve<int32_t>(cur, E);
+  w.offsets = carve<int32_t>(cur, E + 1);
+  w.active = carve<int32_t>(cur, E);
+  w.meta = carve<int32_t>(cur, 4);
+  w.perm = carve<int32_t>(cur, T * k);
+  w.slot = carve<int32_t>(cur, T * k);
+  w.inv = carve<int32_t>(cur, T * k);
+  w.h = carve<float>(cur, T * k * I);
+  w.y = carve<float>(cur, T * k * H);
+  w.x_stage = carve<uint16_t>(cur, T * H);
+  w.out_stage = carve<uint16_t>(cur, T * H);
+  w.err = carve<uint32_t>(cur, 1);
+  if (ws) *ws = w;
+  return (size_t)(cur - base);
+}
+
+size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t** gu_c, uint8_t** gu_s,
+                      uint8_t** dn_c, uint8_t** dn_s, float** rw, float** rb, float** gug, float** dng) {
+  const size_t E = c.n_experts, H = c.hidden, I = c.inter;
+  char* cur = base;
+  *rw = carve<float>(cur, H * E);
+  *rb = carve<float>(cur, E);
+  *gug = carve<float>(cur, 2 * E);
+  *dng = carve<float>(cur, E);
+  *gu_c = carve<uint8_t>(cur, E * 2 * I * (H / 2));
+  *gu_s = carve<uint8_t>(cur, E * 2 * I * (H / 16));
+  *dn_c = carve<uint8_t>(cur, E * H * (I / 2));
+  *dn_s = carve<uint8_t>(cur, E * H * (I / 16));
+  if (L) {
+    L->router_w = *rw;
+    L->router_bias = *rb;
+    L->gu_global = *gug;
+    L->dn_global = *dng;
+    L->gu_codes = *gu_c;
+    L->gu_scales = *gu_s;
+    L->dn_codes = *dn_c;
+    L->dn_scales = *dn_s;
+  }
+  return (size_t)(cur - base);
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Events bracketing one stage of a profiled forward (no-ops when not armed).
+struct StageTimer {
+  moe_ctx* ctx;
+  cudaStream_t s;
+  int call;
+  StageTimer(moe_ctx* c, cudaStream_t st) : ctx(c), s(st), call(-1) {
+    if (ctx->prof_max > 0 && ctx->prof_calls < ctx->prof_max) call = ctx->prof_calls++;
+  }
+  void begin(int stage) {
+    if (call >= 0) cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s);
+  }
+  void end(int stage) {
+    if (call >= 0) cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 1], s);
+  }
+};
+
+int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm) {
+  cudaError_t e;
+  if (tm) tm->begin(kStageRouter);
+  e = launch_router(ctx->sh, ctx->L, ctx->ws, x, T, ctx->sm_count, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageRouter);
+  if (tm) tm->begin(kStageSelect);
+  e = launch_select(ctx->sh, ctx->ws.logits, ctx->ws.idx, ctx->ws.w, T, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageSelect);
+  if (tm) tm->begin(kStagePermute);
+  e = launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStagePermute);
+  ctx->launches += 6;
+  return MOE_OK;
+}
+
+int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, StageTimer* tm) {
+  cudaError_t e;
+  if (tm) tm->begin(kStageGateUp);
+  e = launch_gateup_simt(ctx->sh, ctx->L, ctx->ws, x, T, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageGateUp);
+  if (tm) tm->begin(kStageDown);
+  e = launch_down_simt(ctx->sh, ctx->L, ctx->ws, T, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageDown);
+  if (tm) tm->begin(kStageCombine);
+  e = launch_combine(ctx->sh, ctx->ws, out, T, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageCombine);
+  ctx->launches += 3;
+  return MOE_OK;
+}
+
+int check_forward_args(moe_ctx* ctx, const void* x, const void* out, int32_t T) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)T * ctx->cfg.hidden * 2;
+  const char* xa = (const char*)x;
+  const char* oa = (const char*)out;
+  if (xa < oa + bytes && oa < xa + bytes) return MOE_ERR_INVALID_ARG;
+  if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case MOE_ERR_NOT_LOADED: return "layer not loaded";
+    case MOE_ERR_OOM: return "device out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_FLAG: return "device error flag raised";
+    default: return "unknown status";
+  }
+}
+
+int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (device < 0 || device >= ndev) return MOE_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
+  DeviceGuard g(device);
+  moe_ctx* ctx = new moe_ctx();
+  ctx->cfg = *cfg;
+  ctx->sh = Shape{cfg->hidden, cfg->inter, cfg->n_experts, cfg->top_k};
+  ctx->device = device;
+  ctx->sm_count = prop.multiProcessorCount;
+  ctx->ws_bytes = workspace_layout(*cfg, ctx->sm_count, nullptr, nullptr);
+  if (cudaMalloc(&ctx->ws_mem, ctx->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return MOE_ERR_OOM;
+  }
+  workspace_layout(*cfg, ctx->sm_count, &ctx->ws, (char*)ctx->ws_mem);
+  if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(ctx->ws_mem);
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  *out = ctx;
+  return MOE_OK;
+}
+
+int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
+  if (!ctx || !lh || !lh->router_w || !lh->gu_codes || !lh->gu_scales || !lh->gu_global || !lh->dn_codes ||
+      !lh->dn_scales || !lh->dn_global)
+    return MOE_ERR_INVALID_ARG;
+  const moe_config& c = ctx->cfg;
+  const size_t E = c.n_experts, H = c.hidden, I = c.inter;
+  for (size_t e = 0; e < E; ++e)
+    if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  uint8_t *gu_c, *gu_s, *dn_c, *dn_s;
+  float *rw, *rb, *gug, *dng;
+  if (!ctx->weights_mem) {
+    ctx->weights_bytes = weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng);
+    if (cudaMalloc(&ctx->weights_mem, ctx->weights_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      ctx->weights_mem = nullptr;
+      return MOE_ERR_OOM;
+    }
+  }
+  ctx->loaded = false;
+  weights_layout(c, &ctx->L, (char*)ctx->weights_mem, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng);
+  const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
+  uint8_t* staging = nullptr;
+  if (cudaMalloc(&staging, gu_cb + gu_sb + dn_cb + dn_sb) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_OOM;
+  }
+  cudaStream_t s;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(staging);
+    return MOE_ERR_CUDA;
+  }
+  int st = MOE_OK;
+  do {
+    if (cudaMemcpy(rw, lh->router_w, H * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    if (lh->router_bias) {
+      if (cudaMemcpy(rb, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    } else if (cudaMemset(rb, 0, E * sizeof(float)) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    if (cudaMemcpy(gug, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    if (cudaMemcpy(dng, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    for (size_t e = 0; e < E && st == MOE_OK; ++e) {
+      if (cudaStreamSynchronize(s) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+      uint8_t* sc = staging;
+      uint8_t* ss = staging + gu_cb;
+      uint8_t* dc = ss + gu_sb;
+      uint8_t* ds = dc + dn_cb;
+      if (cudaMemcpyAsync(sc, lh->gu_codes[e], gu_cb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(ss, lh->gu_scales[e], gu_sb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(dc, lh->dn_codes[e], dn_cb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          cudaMemcpyAsync(ds, lh->dn_scales[e], dn_sb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        st = MOE_ERR_CUDA;
+        break;
+      }
+      if (launch_repack_expert(ctx->sh, (int)e, sc, ss, dc, ds, gu_c, gu_s, dn_c, dn_s, s) != cudaSuccess) {
+        st = MOE_ERR_CUDA;
+        break;
+      }
+    }
+    if (st == MOE_OK && cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
+  } while (0);
+  cudaStreamDestroy(s);
+  cudaFree(staging);
+  if (st == MOE_OK) ctx->loaded = true;
+  return st;
+}
+
+int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T) {
+  int st = check_forward_args(ctx, x, out, T);
+  if (st != MOE_OK || T == 0) return st;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  StageTimer tm(ctx, s);
+  st = run_route(ctx, s, (const uint16_t*)x, T, &tm);
+  if (st != MOE_OK) return st;
+  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, &tm);
+}
+
+int moe_forward_host(moe_ctx* ctx, void* stream, const void* x_host, void* out_host, int32_t T) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)T * ctx->cfg.hidden * 2;
+  if (cudaMemcpyAsync(ctx->ws.x_stage, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  int st = moe_forward(ctx, stream, ctx->ws.x_stage, ctx->ws.out_stage, T);
+  if (st != MOE_OK) return st;
+  if (cudaMemcpyAsync(out_host, ctx->ws.out_stage, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return MOE_OK;
+  DeviceGuard g(ctx->device);
+  for (cudaEvent_t ev : ctx->prof_ev) cudaEventDestroy(ev);
+  if (ctx->weights_mem) cudaFree(ctx->weights_mem);
+  if (ctx->ws_mem) cudaFree(ctx->ws_mem);
+  delete ctx;
+  return MOE_OK;
+}
+
+int moe_get_error(moe_ctx* ctx, uint32_t* bits) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  uint32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, ctx->ws.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ctx->ws.err, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? MOE_ERR_DEVICE_FLAG : MOE_OK;
+}
+
+static int copy_route_outputs(moe_ctx* ctx, cudaStream_t s, int T, float* logits, int32_t* idx, float* w,
+                              int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
+  const size_t E = ctx->cfg.n_experts, k = ctx->cfg.top_k;
+  struct Item { void* dst; const void* src; size_t bytes; } items[] = {
+      {logits, ctx->ws.logits, (size_t)T * E * 4}, {idx, ctx->ws.idx, (size_t)T * k * 4},
+      {w, ctx->ws.w, (size_t)T * k * 4},           {offsets, ctx->ws.offsets, (E + 1) * 4},
+      {perm, ctx->ws.perm, (size_t)T * k * 4},     {slot, ctx->ws.slot, (size_t)T * k * 4},
+      {inv, ctx->ws.inv, (size_t)T * k * 4}};
+  for (const Item& it : items)
+    if (it.dst && cudaMemcpyAsync(it.dst, it.src, it.bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_debug_route(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* logits, int32_t* idx, float* w,
+                    int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
+  if (!ctx || !x || T <= 0 || T > ctx->cfg.max_tokens || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr);
+  if (st != MOE_OK) return st;
+  return copy_route_outputs(ctx, s, T, logits, idx, w, offsets, perm, slot, inv);
+}
+
+int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, int32_t T, int32_t* idx, float* w,
+                     int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
+  if (!ctx || !logits || T <= 0 || T > ctx->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_select(ctx->sh, logits, ctx->ws.idx, ctx->ws.w, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return copy_route_outputs(ctx, s, T, nullptr, idx, w, offsets, perm, slot, inv);
+}
+
+int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y) {
+  if (!ctx || !x || T <= 0 || T > ctx->cfg.max_tokens || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr);
+  if (st != MOE_OK) return st;
+  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, nullptr);
+  if (st != MOE_OK) return st;
+  const size_t rows = (size_t)T * ctx->cfg.top_k;
+  if (h && cudaMemcpyAsync(h, ctx->ws.h, rows * ctx->cfg.inter * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (y && cudaMemcpyAsync(y, ctx->ws.y, rows * ctx->cfg.hidden * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_profile_stages(void) { return kNumStages; }
+
+const char* moe_profile_stage_name(int i) { return (i >= 0 && i < kNumStages) ? kStageNames[i] : ""; }
+
+int moe_profile_begin(moe_ctx* ctx, int32_t max_calls) {
+  if (!ctx || max_calls < 0) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  for (cudaEvent_t ev : ctx->prof_ev) cudaEventDestroy(ev);
+  ctx->prof_ev.assign((size_t)max_calls * kNumStages * 2, nullptr);
+  for (auto& ev : ctx->prof_ev)
+    if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
+  ctx->prof_max = max_calls;
+  ctx->prof_calls = 0;
+  return MOE_OK;
+}
+
+int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n) {
+  if (!ctx || n < 0 || n > kNumStages) return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  for (int i = 0; i < n; ++i) {
+    if (ms) ms[i] = 0.f;
+    if (launches) launches[i] = 0;
+  }
+  for (int c = 0; c < ctx->prof_calls; ++c)
+    for (int i = 0; i < n; ++i) {
+      cudaEvent_t a = ctx->prof_ev[((size_t)c * kNumStages + i) * 2], b = ctx->prof_ev[((size_t)c * kNumStages + i) * 2 + 1];
+      if (cudaEventSynchronize(b) != cudaSuccess) return MOE_ERR_CUDA;
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, a, b) != cudaSuccess) return MOE_ERR_CUDA;
+      if (ms) ms[i] += t;
+      if (launches) launches[i] += 1;
+    }
+  ctx->prof_max = 0;
+  ctx->prof_calls = 0;
+  return MOE_OK;
+}
+
+int64_t moe_launch_count(const moe_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+int64_t moe_device_bytes(const moe_ctx* ctx) {
+  if (!ctx) return 0;
+  return (int64_t)(ctx->weights_bytes + ctx->ws_bytes);
+}
+
+}  // extern "C"

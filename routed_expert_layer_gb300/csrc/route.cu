@@ -1,0 +1,308 @@
+// Routing: router logits (S1), top-k select with renormalised softmax weights (S2),
+// and the histogram / prefix-sum / stable permutation into per-expert groups (S3).
+//
+// S1: each token is scored against every expert ("Kimi-K3 NVFP4 station eight
+//     sparks", section "The number the project hangs on": attention, then a router,
+//     then 16 experts, then a sum). fp32 logits, deterministic: a fixed K split and
+//     a fixed-order reduction of the partial sums.
+// S2: 16 of 896 experts per token ("Serving Kimi-K3 ... with 8xB300 GPUs", section
+//     "The model, as the serving system sees it"). Order: logit descending, expert
+//     index ascending, -0 == +0; made total by a 64-bit key so the result is unique.
+// S3: route records sorted by expert, stable in token order (SemiAnalysis essay,
+//     sections 4 and 15: build records, count, permute, later restore token order).
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// ---- S1 router -----------------------------------------------------------------------
+
+int router_splits(const Shape& sh, int T, int sm_count) {
+  const int tiles = ((T + kRouterTT - 1) / kRouterTT) * ((sh.E + kRouterTE - 1) / kRouterTE);
+  const int max_s = sh.H / 64;
+  int s = (2 * sm_count + tiles - 1) / tiles;
+  if (s < 1) s = 1;
+  if (s > max_s) s = max_s;
+  if (s > 64) s = 64;
+  // round the slice to whole 64-row chunks, then recount the splits
+  const int ks = ((sh.H / s + 63) / 64) * 64;
+  return (sh.H + ks - 1) / ks;
+}
+
+static int router_slice(const Shape& sh, int S) { return ((sh.H / S + 63) / 64) * 64; }
+
+size_t router_part_elems(const Shape& sh, int T_max, int sm_count) {
+  size_t best = 0;
+  // splits shrink as T grows; the product S*T peaks where S first drops below its cap
+  for (int T = 1; T <= T_max; T = (T < 64 ? T + 1 : T + kRouterTT)) {
+    size_t v = (size_t)router_splits(sh, T, sm_count) * (size_t)T * (size_t)sh.E;
+    if (v > best) best = v;
+  }
+  size_t v = (size_t)router_splits(sh, T_max, sm_count) * (size_t)T_max * (size_t)sh.E;
+  return v > best ? v : best;
+}
+
+// grid (ceil(T/16), ceil(E/128), S), block 128: thread = expert column, 16 token rows
+// held in registers; x is staged in shared memory 64 rows of K at a time.
+__global__ void __launch_bounds__(kRouterTE) router_partial_kernel(const uint16_t* __restrict__ x,
+                                                                    const float* __restrict__ W,
+                                                                    float* __restrict__ part, int T, int H, int E,
+                                                                    int KS) {
+  __shared__ float xs[64][kRouterTT];
+  const int t0 = blockIdx.x * kRouterTT;
+  const int e = blockIdx.y * kRouterTE + threadIdx.x;
+  const int s = blockIdx.z;
+  const int h0 = s * KS;
+  const int h1 = min(H, h0 + KS);
+  float acc[kRouterTT];
+#pragma unroll
+  for (int i = 0; i < kRouterTT; ++i) acc[i] = 0.f;
+  for (int hc = h0; hc < h1; hc += 64) {
+    for (int i = threadIdx.x; i < 64 * kRouterTT; i += kRouterTE) {
+      const int tt = i / 64, r = i % 64;
+      float v = 0.f;
+      if (t0 + tt < T) {
+        const uint32_t b = x[(size_t)(t0 + tt) * H + hc + r];
+        v = __uint_as_float(b << 16);
+      }
+      xs[r][tt] = v;
+    }
+    __syncthreads();
+    if (e < E) {
+#pragma unroll 8
+      for (int r = 0; r < 64; ++r) {
+        const float wv = __ldg(W + (size_t)(hc + r) * E + e);
+        const float4* xr = reinterpret_cast<const float4*>(&xs[r][0]);
+#pragma unroll
+        for (int q = 0; q < kRouterTT / 4; ++q) {
+          const float4 xv = xr[q];
+          acc[4 * q + 0] = fmaf(xv.x, wv, acc[4 * q + 0]);
+          acc[4 * q + 1] = fmaf(xv.y, wv, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(xv.z, wv, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(xv.w, wv, acc[4 * q + 3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (e < E) {
+#pragma unroll
+    for (int tt = 0; tt < kRouterTT; ++tt)
+      if (t0 + tt < T) part[((size_t)s * T + t0 + tt) * E + e] = acc[tt];
+  }
+}
+
+// logits[t][e] = sum over splits s ascending of part[s][t][e], plus bias[e].
+__global__ void router_reduce_kernel(const float* __restrict__ part, const float* __restrict__ bias,
+                                     float* __restrict__ logits, int T, int E, int S) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t n = (size_t)T * E;
+  if (i >= n) return;
+  float acc = 0.f;
+  for (int s = 0; s < S; ++s) acc += part[(size_t)s * n + i];
+  logits[i] = acc + bias[i % E];
+}
+
+cudaError_t launch_router(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
+                          int sm_count, cudaStream_t s) {
+  const int S = router_splits(sh, T, sm_count);
+  const int KS = router_slice(sh, S);
+  dim3 grid((T + kRouterTT - 1) / kRouterTT, (sh.E + kRouterTE - 1) / kRouterTE, S);
+  router_partial_kernel<<<grid, kRouterTE, 0, s>>>(x, L.router_w, ws.router_part, T, sh.H, sh.E, KS);
+  const size_t n = (size_t)T * sh.E;
+  router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.router_part, L.router_bias, ws.logits, T,
+                                                                    sh.E, S);
+  return cudaGetLastError();
+}
+
+// ---- S2 select ---------------------------------------------------------------------------
+
+// Order-preserving map of an fp32 logit to uint32 (larger float -> larger key);
+// -0 is folded onto +0 so the two compare equal.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp per token. Each lane holds the keys of experts lane, lane+32, ... as
+// (ordered logit << 32) | (0xFFFFFFFF - e): all keys distinct, the largest key is
+// the largest logit with the lowest index. k rounds of a warp-wide max.
+__global__ void select_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
+                              int T, int E, int k) {
+  const int tok = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= T) return;
+  const float* l = logits + (size_t)tok * E;
+  unsigned long long keys[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    keys[i] = (e < E) ? (((unsigned long long)ordered_bits(l[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e))
+                      : 0ull;
+  }
+  uint32_t taken = 0;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0ull;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (!((taken >> i) & 1u) && keys[i] > best) {
+        best = keys[i];
+        bi = i;
+      }
+    }
+    unsigned long long m = best;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+      m = (o > m) ? o : m;
+    }
+    if (bi >= 0 && best == m) taken |= 1u << bi;
+    if (lane == j) my_e = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
+  }
+  const float v = (lane < k) ? l[my_e] : 0.f;
+  const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+  float p = (lane < k) ? expf(v - m0) : 0.f;
+  float sum = p;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+  if (lane < k) {
+    idx[(size_t)tok * k + lane] = my_e;
+    w[(size_t)tok * k + lane] = p / sum;
+  }
+}
+
+cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s) {
+  const int warps_per_block = 8;
+  const int blocks = (T + warps_per_block - 1) / warps_per_block;
+  select_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(logits, idx, w, T, sh.E, sh.k);
+  return cudaGetLastError();
+}
+
+// ---- S3 histogram / prefix sum / permutation --------------------------------------------------
+
+// Per 32-token chunk c and expert e: mask[c][e] bit i set iff token 32c+i chose e.
+// 256 threads = 8 chunks; atomicOr makes the masks independent of thread order.
+__global__ void __launch_bounds__(256) perm_masks_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ masks,
+                                                         uint32_t* __restrict__ err, int T, int E, int k) {
+  extern __shared__ uint32_t msk[];  // [8][E]
+  for (int i = threadIdx.x; i < 8 * E; i += 256) msk[i] = 0u;
+  __syncthreads();
+  const int cl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 256 + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)t * k + j];
+      if (e < 0 || e >= E) {
+        atomicOr(err, kErrExpertRange);
+        continue;
+      }
+      atomicOr(&msk[cl * E + e], 1u << lane);
+    }
+  }
+  __syncthreads();
+  const int C = (T + 31) / 32;
+  for (int i = threadIdx.x; i < 8 * E; i += 256) {
+    const int c = blockIdx.x * 8 + i / E;
+    if (c < C) masks[(size_t)c * E + (i % E)] = msk[i];
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int ws = warp_sums[lane];
+    int wi = ws;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    warp_sums[lane] = wi - ws;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_sums[wid] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// One CTA of 1024 threads; thread e walks the chunks in order: chunk_base[c][e] =
+// rows of e in chunks before c; counts, offsets (exclusive scan over e) and the
+// ascending list of touched experts.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restrict__ masks,
+                                                         int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                                                         int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+                                                         int32_t* __restrict__ meta, int T, int E) {
+  __shared__ int totals[2];
+  __shared__ int max_rows;
+  const int e = threadIdx.x;
+  const int C = (T + 31) / 32;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < C; ++c) {
+      const uint32_t mk = masks[(size_t)c * E + e];
+      chunk_base[(size_t)c * E + e] = run;
+      run += __popc(mk);
+    }
+    counts[e] = run;
+  }
+  if (threadIdx.x == 0) max_rows = 0;
+  __syncthreads();
+  if (run > 0) atomicMax(&max_rows, run);
+  const int off = block_exclusive_scan(run, &totals[0]);
+  const int pos = block_exclusive_scan(run > 0 ? 1 : 0, &totals[1]);
+  if (e < E) {
+    offsets[e] = off;
+    if (run > 0) active[pos] = e;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = totals[0];
+    meta[0] = totals[1];
+    meta[1] = max_rows;
+  }
+}
+
+// Thread per (t, j): p = offsets[e] + rows of e in earlier chunks + earlier tokens of this chunk.
+__global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restrict__ masks,
+                                    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                                    int32_t* __restrict__ perm, int32_t* __restrict__ slot, int32_t* __restrict__ inv,
+                                    int T, int E, int k) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * k) return;
+  const int t = i / k, j = i % k;
+  const int e = idx[i];
+  if (e < 0 || e >= E) {
+    inv[i] = -1;
+    return;
+  }
+  const int c = t >> 5, lane = t & 31;
+  const uint32_t mk = masks[(size_t)c * E + e];
+  const int p = offsets[e] + chunk_base[(size_t)c * E + e] + __popc(mk & ((1u << lane) - 1u));
+  perm[p] = t;
+  slot[p] = j;
+  inv[i] = p;
+}
+
+cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s) {
+  const int blocks = (T + 255) / 256;
+  perm_masks_kernel<<<blocks, 256, 8 * sh.E * sizeof(uint32_t), s>>>(idx, ws.masks, ws.err, T, sh.E, sh.k);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(ws.masks, ws.chunk_base, ws.counts, ws.offsets, ws.active, ws.meta, T, sh.E);
+  const int n = T * sh.k;
+  perm_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(idx, ws.masks, ws.chunk_base, ws.offsets, ws.perm, ws.slot,
+                                                      ws.inv, T, sh.E, sh.k);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,83 @@
+"""The layer at the K3 shape (H=7168, I=1536, E=896, k=16, NVFP4 experts of
+18,579,480 bytes, 16.6 GB per layer) on the GPU, in the launch configuration the
+benchmark times: decode T=1, 8, 53; verify/batched decode T=64, 128, 256;
+prefill T=2048, 4096, 8192; Zipf(1.1)-skewed routing at T=64 and 4096.
+
+Sampled output rows are checked against the oracle token by token (each row
+depends only on its own token); the permutation is checked by properties that
+hold at any size; the selection at full size is checked bit-exactly in
+test_gpu_select.py."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import SHAPES, check_output, check_routing, gpu_forward, gpu_route, layer
+
+pytestmark = pytest.mark.gpu
+
+K3 = SHAPES["k3"]
+T_MAX = 8192
+
+
+@pytest.fixture(scope="module")
+def k3():
+    import routed_expert_layer_gb300 as rel
+    m = rel.MoeLayer(K3["H"], K3["I"], K3["E"], K3["k"], T_MAX)
+    m.load(layer("k3"))
+    yield m
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def k3_zipf():
+    import routed_expert_layer_gb300 as rel
+    m = rel.MoeLayer(K3["H"], K3["I"], K3["E"], K3["k"], 4096)
+    m.load(layer("k3", zipf=True))
+    yield m
+    m.close()
+
+
+def sample_rows(T, n=5, seed=0):
+    rng = np.random.default_rng(seed + T)
+    rows = {0, T - 1, T // 2} | set(rng.integers(0, T, size=n).tolist())
+    return np.array(sorted(rows))
+
+
+def check_permutation_properties(r, T, E, k):
+    offs, perm, slot, inv = r["offsets"], r["perm"], r["slot"], r["inv"]
+    counts = np.diff(offs)
+    assert offs[0] == 0 and offs[-1] == T * k and np.all(counts >= 0)
+    assert np.array_equal(np.bincount(perm, minlength=T), np.full(T, k))
+    assert np.array_equal(inv[perm * k + slot], np.arange(T * k))
+    e_of_row = np.repeat(np.arange(E), counts)
+    assert np.array_equal(r["idx"].reshape(-1)[perm * k + slot], e_of_row)
+    for e in np.nonzero(counts > 1)[0][:200]:  # stable: tokens ascending inside a bucket
+        assert np.all(np.diff(perm[offs[e]:offs[e + 1]]) > 0)
+
+
+def run_k3(moe, T, zipf=False):
+    L = layer("k3", zipf)
+    x = synth.x_bf16(3 + T, T, K3["H"])
+    out = gpu_forward(moe, x)
+    r = gpu_route(moe, x, K3["E"], K3["k"])
+    check_permutation_properties(r, T, K3["E"], K3["k"])
+    rows = sample_rows(T)
+    ref, ref_idx, ref_w, ref_logits = oracle.moe_tokens(oracle.Layer(L), x[rows], K3["k"])
+    ref_abs = oracle.router_abs(x[rows], L.router_w)
+    ties = check_routing(r["logits"][rows], r["idx"][rows], ref_logits, ref_abs, ref_idx, K3["k"])
+    ratio = check_output(out[rows], ref, ~ties)
+    assert moe.get_error() == 0
+    counts = np.diff(r["offsets"])
+    print(f"K3 T={T} zipf={zipf}: touched={int((counts > 0).sum())} max_rows={int(counts.max())} "
+          f"err/rms={ratio:.3e} near_ties={int(ties.sum())}")
+
+
+@pytest.mark.parametrize("T", [1, 8, 53, 64, 128, 256, 2048, 4096, 8192])
+def test_k3_uniform(k3, T):
+    run_k3(k3, T)
+
+
+@pytest.mark.parametrize("T", [64, 4096])
+def test_k3_zipf(k3_zipf, T):
+    run_k3(k3_zipf, T, zipf=True)

@@ -1,0 +1,167 @@
+"""The whole layer on the GPU through the C ABI against the oracle, at sizes the
+oracle finishes in seconds: the tiny configuration (T=4, H=256, I=128, E=32, k=4)
+and a mid shape spanning several tiles with ragged token counts; plus the ABI's
+edge cases (T=0, T=max, bad pointers, forward before load), determinism, the
+host-buffer entry point and the stage hooks."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (SHAPES, bf16_bits_to_f64, check_output, check_routing, gpu_forward, gpu_route, layer)
+
+pytestmark = pytest.mark.gpu
+
+
+def make(name, max_tokens, zipf=False):
+    import routed_expert_layer_gb300 as rel
+    s = SHAPES[name]
+    m = rel.MoeLayer(s["H"], s["I"], s["E"], s["k"], max_tokens)
+    m.load(layer(name, zipf))
+    return m
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    m = make("tiny", 64)
+    yield m
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def mid():
+    m = make("mid", 512)
+    yield m
+    m.close()
+
+
+def run_case(moe, name, T, seed, zipf=False):
+    s = SHAPES[name]
+    L = layer(name, zipf)
+    x = synth.x_bf16(seed, T, s["H"])
+    ref, ref_idx, ref_w, ref_logits = oracle.moe_forward(oracle.Layer(L), x, s["k"])
+    r = gpu_route(moe, x, s["E"], s["k"])
+    ref_abs = oracle.router_abs(x, L.router_w)
+    ties = check_routing(r["logits"], r["idx"], ref_logits, ref_abs, ref_idx, s["k"])
+    out = gpu_forward(moe, x)
+    ratio = check_output(out, ref, ~ties)
+    assert moe.get_error() == 0
+    return ratio
+
+
+def test_tiny_config(tiny):
+    """The tiny configuration exactly: T=4, H=256, I=128, E=32, k=4, seed 3."""
+    run_case(tiny, "tiny", 4, 3)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 33, 64])
+def test_tiny_sizes(tiny, T):
+    run_case(tiny, "tiny", T, 100 + T)
+
+
+@pytest.mark.parametrize("T", [1, 7, 37, 300, 512])
+def test_mid_sizes(mid, T):
+    run_case(mid, "mid", T, 200 + T)
+
+
+def test_mid_zipf_routing():
+    m = make("mid", 300, zipf=True)
+    try:
+        run_case(m, "mid", 300, 77, zipf=True)
+    finally:
+        m.close()
+
+
+def test_expert_stage_h_and_y(mid):
+    """h (SwiGLU) and y (down projection) per routed row against the oracle's expert functions."""
+    import torch
+    s = SHAPES["mid"]
+    L = layer("mid")
+    OL = oracle.Layer(L)
+    T, k = 9, s["k"]
+    x = synth.x_bf16(55, T, s["H"])
+    r = gpu_route(mid, x, s["E"], k)
+    h = torch.empty(T * k, s["I"], dtype=torch.float32, device="cuda")
+    y = torch.empty(T * k, s["H"], dtype=torch.float32, device="cuda")
+    mid.debug_experts(torch.from_numpy(x.view(np.int16)).cuda(), h=h, y=y)
+    torch.cuda.synchronize()
+    h, y = h.cpu().numpy().astype(np.float64), y.cpu().numpy().astype(np.float64)
+    xf = bf16_bits_to_f64(x)
+    offs = r["offsets"]
+    for e in np.nonzero(np.diff(offs))[0]:
+        rows = np.arange(offs[e], offs[e + 1])
+        toks = r["perm"][rows]
+        href = oracle.expert_gateup(OL, int(e), xf[toks])
+        yref = oracle.expert_down(OL, int(e), href)
+        check_output(h[rows], href, tol=2e-5)
+        check_output(y[rows], oracle.expert_down(OL, int(e), h[rows]), tol=2e-5)
+        check_output(y[rows], yref, tol=1e-4)
+
+
+def test_zero_tokens_is_a_noop(tiny):
+    import torch
+    import routed_expert_layer_gb300 as rel
+    x = torch.zeros(0, 256, dtype=torch.int16, device="cuda")
+    tiny.forward(x, torch.zeros(0, 256, dtype=torch.int16, device="cuda"))
+    assert rel.lib().moe_forward(tiny.ctx, None, None, None, 0) == 0
+
+
+def test_max_tokens_and_beyond(tiny):
+    import torch
+    import routed_expert_layer_gb300 as rel
+    run_case(tiny, "tiny", 64, 9)
+    x = torch.zeros(65, 256, dtype=torch.int16, device="cuda")
+    with pytest.raises(rel.MoeError) as ei:
+        tiny.forward(x, torch.zeros_like(x))
+    assert ei.value.status == rel.MOE_ERR_INVALID_ARG
+
+
+def test_bad_pointers_rejected(tiny):
+    import ctypes
+    import torch
+    import routed_expert_layer_gb300 as rel
+    L = rel.lib()
+    buf = torch.zeros(3 * 256 + 8, dtype=torch.int16, device="cuda")
+    base = buf.data_ptr()
+    # misaligned
+    assert L.moe_forward(tiny.ctx, None, ctypes.c_void_p(base + 2), ctypes.c_void_p(base + 2048), 1) == rel.MOE_ERR_INVALID_ARG
+    # out overlaps x
+    assert L.moe_forward(tiny.ctx, None, ctypes.c_void_p(base), ctypes.c_void_p(base + 256), 1) == rel.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(tiny.ctx, None, None, ctypes.c_void_p(base), 1) == rel.MOE_ERR_INVALID_ARG
+    assert tiny.get_error() == 0
+
+
+def test_forward_before_load():
+    import torch
+    import routed_expert_layer_gb300 as rel
+    m = rel.MoeLayer(256, 128, 32, 4, 4)
+    try:
+        x = torch.zeros(2, 256, dtype=torch.int16, device="cuda")
+        with pytest.raises(rel.MoeError) as ei:
+            m.forward(x, torch.zeros_like(x))
+        assert ei.value.status == rel.MOE_ERR_NOT_LOADED
+    finally:
+        m.close()
+
+
+def test_deterministic_and_host_entry_point(mid):
+    import torch
+    x = synth.x_bf16(999, 300, 512)
+    a = gpu_forward(mid, x)
+    b = gpu_forward(mid, x)
+    assert np.array_equal(a, b)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    mid.forward_host(xh, oh)
+    assert np.array_equal(bf16_bits_to_f64(oh.numpy().view(np.uint16)), a)
+
+
+def test_profile_hooks(tiny):
+    import torch
+    x = torch.from_numpy(synth.x_bf16(5, 16, 256).view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    tiny.profile_begin(3)
+    for _ in range(3):
+        tiny.forward(x, out)
+    prof = tiny.profile_end()
+    assert prof["gateup"][1] == 3 and prof["gateup"][0] > 0

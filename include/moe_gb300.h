@@ -156,6 +156,37 @@ MOE_API const char* moe_profile_stage_name(int i);
 MOE_API int moe_profile_begin(moe_ctx* ctx, int32_t max_calls);
 MOE_API int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n);
 
+/* ---- routing without allocation ---------------------------------------------- */
+
+/* Limits of moe_route_noalloc (its scratch is a fixed-size array inside the library). */
+#define MOE_NOALLOC_MAX_TOKENS 256
+#define MOE_NOALLOC_MAX_EXPERTS 1024
+#define MOE_NOALLOC_MAX_PARTIALS (1024 * 1024) /* router partial sums, 4-byte words */
+
+/* The routing step (router logits, top-k select, per-expert permutation) for
+ * callers that may not allocate device memory: engines that reserve their whole
+ * HBM budget at start-up and forbid cudaMalloc on the request path, plugin hosts
+ * that only hand out pre-planned buffers, or decode loops that cannot take the
+ * device-wide synchronisation an allocation may cause. The pages have no
+ * counterpart to this call; it adds no new arithmetic, only a different owner for
+ * the scratch memory.
+ * It needs no context and allocates nothing: its scratch (about 5.3 MB) is one
+ * static __device__ array that every GPU loading this library holds until the
+ * process exits. Runs on the CURRENT device, on `stream`.
+ *   x          device bf16 [T][H], 16-byte aligned
+ *   router_w   device fp32 [H][E]; router_bias device fp32 [E] or NULL
+ *   idx, w, offsets, perm, slot, inv: device outputs, caller-allocated, laid out
+ *              as for moe_debug_route (all required)
+ * Limits: H % 64 == 0, 1 <= k <= 32, k <= E <= MOE_NOALLOC_MAX_EXPERTS,
+ * 1 <= T <= MOE_NOALLOC_MAX_TOKENS; larger sizes return MOE_ERR_UNSUPPORTED.
+ * The first call on a device looks up the scratch's device address (make it
+ * before any stream capture). All calls share the one array: calls whose GPU work
+ * overlaps (unordered streams) race and corrupt each other's results. The device
+ * error word of this path is internal and cleared on every call. */
+MOE_API int moe_route_noalloc(void* stream, const void* x, const float* router_w, const float* router_bias,
+                              int32_t H, int32_t E, int32_t k, int32_t T, int32_t* idx, float* w, int32_t* offsets,
+                              int32_t* perm, int32_t* slot, int32_t* inv);
+
 /* Number of kernels this context has enqueued so far (all calls that run kernels). */
 MOE_API int64_t moe_launch_count(const moe_ctx* ctx);
 

@@ -19,7 +19,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libmoe_gb300.so")
-_SOURCES = ["api.cu", "route.cu", "expert_simt.cu"]
+_SOURCES = ["api.cu", "route.cu", "expert_simt.cu", "noalloc.cu"]
 _HEADERS = ["moe_internal.cuh"]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -30,7 +30,8 @@ MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_DEVICE_FLAG = -4, -5, -6
 
 EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "moe_destroy", "moe_status_str",
             "moe_get_error", "moe_debug_route", "moe_debug_select", "moe_debug_experts", "moe_profile_stages",
-            "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count"]
+            "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count",
+            "moe_route_noalloc"]
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
@@ -117,8 +118,19 @@ def lib():
         L.moe_device_bytes.argtypes = [vp]
         L.moe_launch_count.restype = ctypes.c_int64
         L.moe_launch_count.argtypes = [vp]
+        L.moe_route_noalloc.argtypes = [vp, p, p, p, i32, i32, i32, i32, p, p, p, p, p, p]
         _lib = L
     return _lib
+
+
+def route_noalloc(x, router_w, router_bias, k, idx, w, offsets, perm, slot, inv, stream=None) -> None:
+    """Routing without any device allocation (see moe_route_noalloc in the header):
+    every argument is a CUDA tensor on the current device; outputs are caller-allocated."""
+    T, H = x.shape
+    E = router_w.shape[1]
+    _check(lib().moe_route_noalloc(_stream(stream), _dptr(x), _dptr(router_w), _dptr(router_bias), H, E, k, T,
+                                   _dptr(idx), _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
+           "moe_route_noalloc")
 
 
 class MoeError(RuntimeError):

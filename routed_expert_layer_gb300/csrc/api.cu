@@ -1,8 +1,10 @@
 // C ABI: context, weight loading, the forward launch sequence, inspection hooks.
 // The operations and their sources are documented in include/moe_gb300.h.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "moe_internal.cuh"
@@ -22,10 +24,14 @@ struct moe_ctx {
   void* ws_mem = nullptr;
   size_t ws_bytes = 0;
   int64_t launches = 0;  // kernels enqueued by forward calls
+  bool simt = false;     // streaming SIMT expert kernels instead of the tensor-core path
+  CUtensorMap tmap_x{};  // f16 activation rows (B of the gate/up GEMM)
+  CUtensorMap tmap_h{};  // f16 SwiGLU rows (B of the down GEMM)
   // profiling
   int prof_max = 0;
   int prof_calls = 0;
   std::vector<cudaEvent_t> prof_ev;  // [prof_max][kNumStages][2]
+  std::vector<uint8_t> prof_rec;     // [prof_max][kNumStages]: stage ran in that call
 };
 
 namespace {
@@ -41,7 +47,32 @@ struct DeviceGuard {
   }
 };
 
-const char* kStageNames[kNumStages] = {"router", "select", "permute", "gateup", "down", "combine"};
+const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep",
+                                       "gateup", "finalize", "down", "combine"};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 2D f16 tensor [rows][cols] read in boxes of 64 columns x 16 rows with 128-byte swizzle.
+bool make_tmap_f16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+  static EncodeTiledFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int check_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -84,16 +115,38 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.slot = carve<int32_t>(cur, T * k);
   w.inv = carve<int32_t>(cur, T * k);
   w.h = carve<float>(cur, T * k * I);
-  w.y = carve<float>(cur, T * k * H);
   w.x_stage = carve<uint16_t>(cur, T * H);
   w.out_stage = carve<uint16_t>(cur, T * H);
   w.err = carve<uint32_t>(cur, 1);
+  // tensor-core path: sizes are the maxima over every T <= max_tokens of its plan
+  size_t part1 = 0, ytc = T * k * H, cap1 = 0, cap2 = 0;
+  for (int t = 1; t <= c.max_tokens; ++t) {
+    const TcPlan pl = tc_plan(sh, t, sm_count);
+    const size_t rows = (size_t)t * k;
+    if (pl.S1 > 1) part1 = std::max(part1, (size_t)pl.S1 * rows * 2 * I);
+    ytc = std::max(ytc, (size_t)pl.S2 * rows * H);
+    cap1 = std::max(cap1, tc_items_cap(sh, t, 1, sm_count));
+    cap2 = std::max(cap2, tc_items_cap(sh, t, 2, sm_count));
+  }
+  w.xg = carve<uint16_t>(cur, T * k * H);
+  w.row_scale = carve<float>(cur, T * k);
+  w.h16 = carve<uint16_t>(cur, T * k * I);
+  w.part1 = carve<float>(cur, std::max<size_t>(part1, 1));
+  w.ytc = carve<float>(cur, ytc);
+  w.y = w.ytc;  // the streaming path's y aliases the same buffer
+  w.items1 = carve<TcItem>(cur, cap1);
+  w.items2 = carve<TcItem>(cur, cap2);
+  w.n_items1 = carve<int32_t>(cur, 1);
+  w.n_items2 = carve<int32_t>(cur, 1);
+  w.cap1 = (int)cap1;
+  w.cap2 = (int)cap2;
   if (ws) *ws = w;
   return (size_t)(cur - base);
 }
 
 size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t** gu_c, uint8_t** gu_s,
-                      uint8_t** dn_c, uint8_t** dn_s, float** rw, float** rb, float** gug, float** dng) {
+                      uint8_t** dn_c, uint8_t** dn_s, float** rw, float** rb, float** gug, float** dng,
+                      uint8_t** gu_tc, uint8_t** dn_tc) {
   const size_t E = c.n_experts, H = c.hidden, I = c.inter;
   char* cur = base;
   *rw = carve<float>(cur, H * E);
@@ -104,7 +157,11 @@ size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t**
   *gu_s = carve<uint8_t>(cur, E * 2 * I * (H / 16));
   *dn_c = carve<uint8_t>(cur, E * H * (I / 2));
   *dn_s = carve<uint8_t>(cur, E * H * (I / 16));
+  *gu_tc = carve<uint8_t>(cur, E * (2 * I / 128) * (H / 64) * 4608);
+  *dn_tc = carve<uint8_t>(cur, E * (H / 128) * (I / 64) * 4608);
   if (L) {
+    L->gu_tc = *gu_tc;
+    L->dn_tc = *dn_tc;
     L->router_w = *rw;
     L->router_bias = *rb;
     L->gu_global = *gug;
@@ -131,7 +188,10 @@ struct StageTimer {
     if (call >= 0) cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s);
   }
   void end(int stage) {
-    if (call >= 0) cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 1], s);
+    if (call >= 0) {
+      cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 1], s);
+      ctx->prof_rec[(size_t)call * kNumStages + stage] = 1;
+    }
   }
 };
 
@@ -153,7 +213,76 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   return MOE_OK;
 }
 
+int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, StageTimer* tm,
+                   TcPlan* plan_out) {
+  const Shape& sh = ctx->sh;
+  const Workspace& ws = ctx->ws;
+  const TcPlan pl = tc_plan(sh, T, ctx->sm_count);
+  if (plan_out) *plan_out = pl;
+  const int rows = T * sh.k;
+  if (tm) tm->begin(kStagePrep);
+  if (launch_gather_x(sh, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_worklist(sh, ws, pl, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStagePrep);
+  TcGemmParams P1;
+  P1.w = ctx->L.gu_tc;
+  P1.M = 2 * sh.I / 128;
+  P1.KC = sh.H / 64;
+  P1.S = pl.S1;
+  P1.items = ws.items1;
+  P1.n_items = ws.n_items1;
+  P1.gscale = ctx->L.gu_global;
+  P1.gstride = 2;
+  P1.gsel = 1;
+  P1.row_scale = ws.row_scale;
+  P1.post_scale = 1.f;
+  P1.mode = pl.S1 == 1 ? kTcModeSwiglu : kTcModePartial;
+  P1.out = ws.part1;
+  P1.out_slice = (size_t)rows * 2 * sh.I;
+  P1.ldo = 2 * sh.I;
+  P1.h16 = ws.h16;
+  P1.I = sh.I;
+  P1.err = ws.err;
+  if (tm) tm->begin(kStageGateUp);
+  if (launch_gemm(pl, ctx->tmap_x, P1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageGateUp);
+  int n = 5;
+  if (pl.S1 > 1) {
+    if (tm) tm->begin(kStageFinalize);
+    if (launch_swiglu_finalize(sh, ws, pl, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tm) tm->end(kStageFinalize);
+    ++n;
+  }
+  TcGemmParams P2;
+  P2.w = ctx->L.dn_tc;
+  P2.M = sh.H / 128;
+  P2.KC = sh.I / 64;
+  P2.S = pl.S2;
+  P2.items = ws.items2;
+  P2.n_items = ws.n_items2;
+  P2.gscale = ctx->L.dn_global;
+  P2.gstride = 1;
+  P2.gsel = 0;
+  P2.row_scale = nullptr;
+  P2.post_scale = kHScale;
+  P2.mode = kTcModePartial;
+  P2.out = ws.ytc;
+  P2.out_slice = (size_t)rows * sh.H;
+  P2.ldo = sh.H;
+  P2.I = sh.I;
+  P2.err = ws.err;
+  if (tm) tm->begin(kStageDown);
+  if (launch_gemm(pl, ctx->tmap_h, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageDown);
+  if (tm) tm->begin(kStageCombine);
+  if (launch_combine_tc(sh, ws, pl, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageCombine);
+  ctx->launches += n;
+  return MOE_OK;
+}
+
 int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, StageTimer* tm) {
+  if (!ctx->simt) return run_experts_tc(ctx, s, x, out, T, tm, nullptr);
   cudaError_t e;
   if (tm) tm->begin(kStageGateUp);
   e = launch_gateup_simt(ctx->sh, ctx->L, ctx->ws, x, T, s);
@@ -230,6 +359,15 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete ctx;
     return MOE_ERR_CUDA;
   }
+  const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
+  if (!make_tmap_f16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden) ||
+      !make_tmap_f16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter)) {
+    cudaFree(ctx->ws_mem);
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  const char* ev = getenv("MOE_GB300_EXPERTS");
+  ctx->simt = ev && strcmp(ev, "simt") == 0;
   *out = ctx;
   return MOE_OK;
 }
@@ -243,10 +381,11 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   for (size_t e = 0; e < E; ++e)
     if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
-  uint8_t *gu_c, *gu_s, *dn_c, *dn_s;
+  uint8_t *gu_c, *gu_s, *dn_c, *dn_s, *gu_tc, *dn_tc;
   float *rw, *rb, *gug, *dng;
   if (!ctx->weights_mem) {
-    ctx->weights_bytes = weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng);
+    ctx->weights_bytes =
+        weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc, &dn_tc);
     if (cudaMalloc(&ctx->weights_mem, ctx->weights_bytes) != cudaSuccess) {
       cudaGetLastError();
       ctx->weights_mem = nullptr;
@@ -254,7 +393,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
     }
   }
   ctx->loaded = false;
-  weights_layout(c, &ctx->L, (char*)ctx->weights_mem, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng);
+  weights_layout(c, &ctx->L, (char*)ctx->weights_mem, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc,
+                 &dn_tc);
   const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
   uint8_t* staging = nullptr;
   if (cudaMalloc(&staging, gu_cb + gu_sb + dn_cb + dn_sb) != cudaSuccess) {
@@ -287,7 +427,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
         st = MOE_ERR_CUDA;
         break;
       }
-      if (launch_repack_expert(ctx->sh, (int)e, sc, ss, dc, ds, gu_c, gu_s, dn_c, dn_s, s) != cudaSuccess) {
+      if (launch_repack_expert(ctx->sh, (int)e, sc, ss, dc, ds, gu_c, gu_s, dn_c, dn_s, s) != cudaSuccess ||
+          launch_repack_tc(ctx->sh, (int)e, sc, ss, dc, ds, gu_tc, dn_tc, s) != cudaSuccess) {
         st = MOE_ERR_CUDA;
         break;
       }
@@ -391,6 +532,12 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   cudaStream_t s = (cudaStream_t)stream;
   int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr);
   if (st != MOE_OK) return st;
+  if (!ctx->simt) {
+    TcPlan pl;
+    st = run_experts_tc(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, nullptr, &pl);
+    if (st != MOE_OK) return st;
+    return launch_debug_hy(ctx->sh, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, nullptr);
   if (st != MOE_OK) return st;
   const size_t rows = (size_t)T * ctx->cfg.top_k;
@@ -410,6 +557,7 @@ int moe_profile_begin(moe_ctx* ctx, int32_t max_calls) {
   DeviceGuard g(ctx->device);
   for (cudaEvent_t ev : ctx->prof_ev) cudaEventDestroy(ev);
   ctx->prof_ev.assign((size_t)max_calls * kNumStages * 2, nullptr);
+  ctx->prof_rec.assign((size_t)max_calls * kNumStages, 0);
   for (auto& ev : ctx->prof_ev)
     if (cudaEventCreate(&ev) != cudaSuccess) return MOE_ERR_CUDA;
   ctx->prof_max = max_calls;
@@ -426,6 +574,7 @@ int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n) {
   }
   for (int c = 0; c < ctx->prof_calls; ++c)
     for (int i = 0; i < n; ++i) {
+      if (!ctx->prof_rec[(size_t)c * kNumStages + i]) continue;
       cudaEvent_t a = ctx->prof_ev[((size_t)c * kNumStages + i) * 2], b = ctx->prof_ev[((size_t)c * kNumStages + i) * 2 + 1];
       if (cudaEventSynchronize(b) != cudaSuccess) return MOE_ERR_CUDA;
       float t = 0.f;

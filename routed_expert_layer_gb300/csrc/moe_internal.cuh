@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -13,9 +14,20 @@ namespace moe {
 // Device error word bits (also documented in moe_get_error).
 constexpr uint32_t kErrExpertRange = 1u;
 constexpr uint32_t kErrCountOverflow = 2u;
+// (bit 4 = a bounded wait in the tensor-core GEMM gave up; see tc_ptx.cuh)
 
 // Profiled stages of one forward.
-enum Stage { kStageRouter = 0, kStageSelect, kStagePermute, kStageGateUp, kStageDown, kStageCombine, kNumStages };
+enum Stage {
+  kStageRouter = 0,
+  kStageSelect,
+  kStagePermute,
+  kStagePrep,      // f16 activation rows + work list
+  kStageGateUp,
+  kStageFinalize,  // K-split reduction + SwiGLU (only when the gate/up GEMM splits K)
+  kStageDown,
+  kStageCombine,
+  kNumStages
+};
 
 // Tokens per pass of the SIMT expert kernels and the SIMT tile shapes.
 constexpr int kSimtNT = 4;        // token rows held in shared memory per pass
@@ -30,6 +42,8 @@ constexpr int kRouterTE = 128;    // router tile: experts (one per thread)
 //   64-element K chunk the 32 rows' 4 scale bytes are contiguous (128 B).
 //   down: tile rt covers output rows 32rt..32rt+31, same chunking along K = I.
 struct DeviceLayer {
+  const uint8_t* gu_tc = nullptr;     // [E][2I/128][H/64][4608] tensor-core tile layout
+  const uint8_t* dn_tc = nullptr;     // [E][H/128][I/64][4608]
   const float* router_w = nullptr;    // [H][E]
   const float* router_bias = nullptr; // [E] (zeros when the caller gave none)
   const uint8_t* gu_codes = nullptr;  // [E][I/16][H/32][32][16]
@@ -38,6 +52,51 @@ struct DeviceLayer {
   const uint8_t* dn_codes = nullptr;  // [E][H/32][I/32][32][16]
   const uint8_t* dn_scales = nullptr; // [E][H/32][I/64][32][4]
   const float* dn_global = nullptr;   // [E]
+};
+
+// ---- tensor-core path ------------------------------------------------------------------
+// h is stored in f16 scaled by 2^-8 (overflow only beyond |h| = 1.6e7; below 2^-6
+// the absolute error stays under 2^-17); the down projection's epilogue undoes it.
+constexpr float kHScaleInv = 1.0f / 256.0f;
+constexpr float kHScale = 256.0f;
+constexpr int kTcDecodeN = 32;        // rows per work item, decode variant
+constexpr int kTcDecodeStages = 10;   // pipeline stages, decode variant (2 CTAs per SM)
+constexpr int kTcPrefillN = 256;      // rows per work item, prefill variant
+constexpr int kTcPrefillStages = 4;   // pipeline stages, prefill variant (1 CTA per SM)
+constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums
+constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes f16 h
+
+struct TcItem {
+  int e;   // expert
+  int p0;  // first routed row
+  int n;   // rows (<= NMAX)
+  int ms;  // (M tile << 8) | K split
+};
+
+struct TcPlan {
+  bool prefill = false;
+  int nmax = kTcDecodeN;
+  int ctas_per_sm = 2;
+  int grid = 0;
+  int S1 = 1, S2 = 1;  // K splits of the gate/up and down GEMMs
+};
+
+struct TcGemmParams {
+  const uint8_t* w = nullptr;        // tile-layout weights [E][M][KC][4608]
+  int M = 0, KC = 0, S = 1;
+  const TcItem* items = nullptr;
+  const int32_t* n_items = nullptr;
+  const float* gscale = nullptr;     // tensor scales
+  int gstride = 1, gsel = 0;         // gscale[e*gstride + (gsel ? row&1 : 0)]
+  const float* row_scale = nullptr;  // per routed row, or null
+  float post_scale = 1.f;
+  int mode = kTcModePartial;
+  float* out = nullptr;              // partial output [S][rows][ldo]
+  size_t out_slice = 0;
+  int ldo = 0;
+  uint16_t* h16 = nullptr;           // SwiGLU output [rows][I]
+  int I = 0;
+  uint32_t* err = nullptr;
 };
 
 struct Workspace {
@@ -59,6 +118,17 @@ struct Workspace {
   uint16_t* x_stage = nullptr;    // [T][H] for moe_forward_host
   uint16_t* out_stage = nullptr;  // [T][H]
   uint32_t* err = nullptr;        // device error word
+  // tensor-core path
+  uint16_t* xg = nullptr;         // [T*k][H] f16 activation rows in routed order
+  float* row_scale = nullptr;     // [T*k] 2^-sigma of each row of xg
+  uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations (x 2^-8)
+  float* part1 = nullptr;         // [S1][T*k][2I] gate/up partial sums (split K only)
+  float* ytc = nullptr;           // [S2][T*k][H] down-projection partial sums
+  TcItem* items1 = nullptr;
+  TcItem* items2 = nullptr;
+  int32_t* n_items1 = nullptr;
+  int32_t* n_items2 = nullptr;
+  int cap1 = 0, cap2 = 0;
 };
 
 struct Shape {
@@ -79,6 +149,20 @@ cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Work
                                cudaStream_t s);
 cudaError_t launch_down_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
 cudaError_t launch_combine(const Shape& sh, const Workspace& ws, uint16_t* out, int T, cudaStream_t s);
+
+TcPlan tc_plan(const Shape& sh, int T, int sm_count);
+size_t tc_items_cap(const Shape& sh, int T, int which, int sm_count);
+cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s);
+cudaError_t launch_worklist(const Shape& sh, const Workspace& ws, const TcPlan& pl, cudaStream_t s);
+cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const TcGemmParams& P, cudaStream_t s);
+cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
+cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
+                              cudaStream_t s);
+cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, float* h, float* y,
+                            cudaStream_t s);
+cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
+                             const uint8_t* dn_codes_raw, const uint8_t* dn_scales_raw, uint8_t* gu_tc, uint8_t* dn_tc,
+                             cudaStream_t s);
 
 // Load-time repack of one expert from raw (caller layout) device staging buffers.
 cudaError_t launch_repack_expert(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,

@@ -119,14 +119,13 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.out_stage = carve<uint16_t>(cur, T * H);
   w.err = carve<uint32_t>(cur, 1);
   // tensor-core path: sizes are the maxima over every T <= max_tokens of its plan
-  size_t part1 = 0, ytc = T * k * H, cap1 = 0, cap2 = 0;
+  size_t part1 = 0, ytc = T * k * H, ccap = 0;
   for (int t = 1; t <= c.max_tokens; ++t) {
     const TcPlan pl = tc_plan(sh, t, sm_count);
     const size_t rows = (size_t)t * k;
     if (pl.S1 > 1) part1 = std::max(part1, (size_t)pl.S1 * rows * 2 * I);
     ytc = std::max(ytc, (size_t)pl.S2 * rows * H);
-    cap1 = std::max(cap1, tc_items_cap(sh, t, 1, sm_count));
-    cap2 = std::max(cap2, tc_items_cap(sh, t, 2, sm_count));
+    ccap = std::max(ccap, tc_chunk_cap(sh, t, sm_count));
   }
   w.xg = carve<uint16_t>(cur, T * k * H);
   w.row_scale = carve<float>(cur, T * k);
@@ -134,12 +133,8 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.part1 = carve<float>(cur, std::max<size_t>(part1, 1));
   w.ytc = carve<float>(cur, ytc);
   w.y = w.ytc;  // the streaming path's y aliases the same buffer
-  w.items1 = carve<TcItem>(cur, cap1);
-  w.items2 = carve<TcItem>(cur, cap2);
-  w.n_items1 = carve<int32_t>(cur, 1);
-  w.n_items2 = carve<int32_t>(cur, 1);
-  w.cap1 = (int)cap1;
-  w.cap2 = (int)cap2;
+  w.chunks = carve<TcChunk>(cur, ccap);
+  w.chunk_cap = (int)ccap;
   if (ws) *ws = w;
   return (size_t)(cur - base);
 }
@@ -157,8 +152,8 @@ size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t**
   *gu_s = carve<uint8_t>(cur, E * 2 * I * (H / 16));
   *dn_c = carve<uint8_t>(cur, E * H * (I / 2));
   *dn_s = carve<uint8_t>(cur, E * H * (I / 16));
-  *gu_tc = carve<uint8_t>(cur, E * (2 * I / 128) * (H / 64) * 4608);
-  *dn_tc = carve<uint8_t>(cur, E * (H / 128) * (I / 64) * 4608);
+  *gu_tc = carve<uint8_t>(cur, E * (2 * I / 128) * (H / 128) * 9216);
+  *dn_tc = carve<uint8_t>(cur, E * (H / 128) * (I / 128) * 9216);
   if (L) {
     L->gu_tc = *gu_tc;
     L->dn_tc = *dn_tc;
@@ -195,7 +190,7 @@ struct StageTimer {
   }
 };
 
-int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm) {
+int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax = 0) {
   cudaError_t e;
   if (tm) tm->begin(kStageRouter);
   e = launch_router(ctx->sh, ctx->L, ctx->ws, x, T, ctx->sm_count, s);
@@ -206,7 +201,7 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageSelect);
   if (tm) tm->begin(kStagePermute);
-  e = launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s);
+  e = launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s, nmax);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePermute);
   ctx->launches += 6;
@@ -222,15 +217,14 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
   const int rows = T * sh.k;
   if (tm) tm->begin(kStagePrep);
   if (launch_gather_x(sh, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_worklist(sh, ws, pl, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePrep);
   TcGemmParams P1;
   P1.w = ctx->L.gu_tc;
   P1.M = 2 * sh.I / 128;
-  P1.KC = sh.H / 64;
+  P1.KC = sh.H / 128;
   P1.S = pl.S1;
-  P1.items = ws.items1;
-  P1.n_items = ws.n_items1;
+  P1.chunks = ws.chunks;
+  P1.n_chunks = ws.meta + 2;
   P1.gscale = ctx->L.gu_global;
   P1.gstride = 2;
   P1.gsel = 1;
@@ -246,7 +240,7 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
   if (tm) tm->begin(kStageGateUp);
   if (launch_gemm(pl, ctx->tmap_x, P1, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageGateUp);
-  int n = 5;
+  int n = 4;
   if (pl.S1 > 1) {
     if (tm) tm->begin(kStageFinalize);
     if (launch_swiglu_finalize(sh, ws, pl, T, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -256,10 +250,10 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
   TcGemmParams P2;
   P2.w = ctx->L.dn_tc;
   P2.M = sh.H / 128;
-  P2.KC = sh.I / 64;
+  P2.KC = sh.I / 128;
   P2.S = pl.S2;
-  P2.items = ws.items2;
-  P2.n_items = ws.n_items2;
+  P2.chunks = ws.chunks;
+  P2.n_chunks = ws.meta + 2;
   P2.gscale = ctx->L.dn_global;
   P2.gstride = 1;
   P2.gsel = 0;
@@ -447,7 +441,8 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
   StageTimer tm(ctx, s);
-  st = run_route(ctx, s, (const uint16_t*)x, T, &tm);
+  const int nmax = ctx->simt ? 0 : tc_plan(ctx->sh, T, ctx->sm_count).nmax;
+  st = run_route(ctx, s, (const uint16_t*)x, T, &tm, nmax);
   if (st != MOE_OK) return st;
   return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, &tm);
 }
@@ -530,7 +525,8 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
-  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr);
+  const int nmax = ctx->simt ? 0 : tc_plan(ctx->sh, T, ctx->sm_count).nmax;
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, nmax);
   if (st != MOE_OK) return st;
   if (!ctx->simt) {
     TcPlan pl;

@@ -39,17 +39,19 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kChunkK = 64;          // K elements per pipeline stage (4 MMAs of K=16)
-constexpr int kRawBytes = 4608;      // one stage of A: 128 rows x 32 B codes + 128 x 4 B scales
-constexpr int kRawSlot = 5120;       // raw slot rounded up to the 1024 B swizzle atom
-constexpr int kBoxRows = 16;         // activation rows per TMA box
+constexpr int kChunkK = 128;         // K elements per pipeline stage (8 MMAs of K=16)
+constexpr int kCodeBytes = 8192;     // one stage of A codes: [4 units of 16 B][128 rows][16 B]
+constexpr int kRawBytes = 9216;      // + scales [128 rows][8 B]
+constexpr int kRawSlot = 10240;      // raw slot rounded up to the 1024 B swizzle atom
+constexpr int kBoxRows = 16;         // activation rows per TMA box (64 f16 = 128 B per row)
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = (2 + kDequantWarps) * 32;
-constexpr int kAStages = 4;          // A tiles in TMEM, 32 columns each
+constexpr int kAStages = 3;          // A tiles in TMEM, 64 columns each
+constexpr int kACols = 64;
 
 __host__ __device__ constexpr uint32_t tmem_cols(int nmax) {
-  const uint32_t need = kAStages * 32 + nmax;
+  const uint32_t need = kAStages * kACols + nmax;
   uint32_t c = 32;
   while (c < need) c <<= 1;
   return c;
@@ -57,23 +59,23 @@ __host__ __device__ constexpr uint32_t tmem_cols(int nmax) {
 
 template <int NMAX, int NS>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /*alignment slack*/ + (size_t)NS * (kRawSlot + NMAX * 128) + 256 /*barriers*/;
+  return 1024 /*alignment slack*/ + (size_t)NS * (kRawSlot + 2 * NMAX * 128) + 256 /*barriers*/;
 }
 
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
-                                                  uint32_t& h3) {
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* h) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
       "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
       "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
       "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
       "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
       : "r"(w));
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_in_low16) {
   uint32_t h;
+  const uint16_t two = (uint16_t)two_in_low16;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
   return h;
 }
@@ -89,15 +91,39 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// 16 codes (one 16-byte unit, one E4M3 scale per 8 of them... two blocks) -> 8 f16x2.
+__device__ __forceinline__ void dequant_unit(const uint4 cw, uint32_t s_lo, uint32_t s_hi, uint32_t* v) {
+  e2m1x8_to_f16x2x4(cw.x, v + 0);
+  e2m1x8_to_f16x2x4(cw.y, v + 4);
+  e2m1x8_to_f16x2x4(cw.z, v + 8);
+  e2m1x8_to_f16x2x4(cw.w, v + 12);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], s_lo);
+#pragma unroll
+  for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], s_hi);
+}
+
+struct Ring {  // stage index and phase parity of a circular buffer of n slots
+  int idx = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 }  // namespace
 
-// Grouped GEMM over the work list. See the file comment for the roles.
+// Grouped GEMM over the work items (chunk, M tile, K split). See the file comment.
 template <int NMAX, int NS>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const TcGemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  constexpr int kStage = kRawSlot + NMAX * 128;
+  constexpr int kBSub = NMAX * 128;          // one 64-column K half of the activation tile
+  constexpr int kStage = kRawSlot + 2 * kBSub;
   constexpr uint32_t kCols = tmem_cols(NMAX);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
@@ -107,7 +133,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accempty = accfull + 1;
   uint64_t* drain = accempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -122,7 +147,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(accfull, 1);
     mbar_init(accempty, kDequantWarps);
     mbar_init(drain, 1);
-    s_fail = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -133,76 +157,89 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t acc_col = kAStages * 32;
-  const int n_items = *P.n_items;
+  constexpr uint32_t acc_col = kAStages * kACols;
+  const int MS = P.M * P.S;
+  const int n_items = *P.n_chunks * MS;
   const int kc_per = P.KC / P.S;
 
   if (warp == 0) {
     // ---- TMA producer ----
     if (lane == 0) {
-      uint32_t g = 0;
+      Ring rs;
+      uint32_t issued = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const TcItem item = P.items[it];
-        const int m = item.ms >> 8, s = item.ms & 0xFF;
-        const int nb = (item.n + kBoxRows - 1) / kBoxRows;
-        const uint8_t* wsrc = P.w + ((size_t)(item.e * P.M + m) * P.KC + (size_t)s * kc_per) * kRawBytes;
-        for (int c = 0; c < kc_per; ++c, ++g) {
-          const int st = g % NS;
-          if (!mbar_wait(&empty[st], ((g / NS) & 1) ^ 1, P.err)) {
+        const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
+        const TcChunk ch = P.chunks[ci];
+        const int nb = (ch.n + kBoxRows - 1) / kBoxRows;
+        const uint8_t* wsrc = P.w + ((size_t)(ch.e * P.M + m) * P.KC + (size_t)s * kc_per) * kRawBytes;
+        const uint32_t tx = kRawBytes + nb * 2 * kBoxBytes;
+        for (int c = 0; c < kc_per; ++c) {
+          if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
             ok = false;
             break;
           }
-          uint8_t* sb = smem + (size_t)st * kStage;
-          mbar_arrive_expect_tx(&full[st], kRawBytes + nb * kBoxBytes);
-          bulk_g2s(sb, wsrc + (size_t)c * kRawBytes, kRawBytes, &full[st]);
+          uint8_t* sb = smem + (size_t)rs.idx * kStage;
+          mbar_arrive_expect_tx(&full[rs.idx], tx);
+          bulk_g2s(sb, wsrc + (size_t)c * kRawBytes, kRawBytes, &full[rs.idx]);
           const int kx = (s * kc_per + c) * kChunkK;
-          for (int b = 0; b < nb; ++b) tma_2d(sb + kRawSlot + b * kBoxBytes, &tmap_b, kx, item.p0 + b * kBoxRows,
-                                              &full[st]);
+          for (int b = 0; b < nb; ++b) {
+            tma_2d(sb + kRawSlot + b * kBoxBytes, &tmap_b, kx, ch.p0 + b * kBoxRows, &full[rs.idx]);
+            tma_2d(sb + kRawSlot + kBSub + b * kBoxBytes, &tmap_b, kx + 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
+          }
+          ++issued;
+          rs.next(NS);
         }
       }
       if (!ok) {
-        s_fail = 1;
         // let copies already issued land before the CTA's shared memory goes away
-        for (uint32_t j = (g > (uint32_t)NS ? g - NS : 0); j < g; ++j) mbar_wait(&full[j % NS], (j / NS) & 1, P.err);
+        Ring w = rs;
+        for (uint32_t j = 0; j < (issued < (uint32_t)NS ? issued : (uint32_t)NS); ++j) {
+          if (w.idx == 0) {
+            w.idx = NS;
+            w.ph ^= 1u;
+          }
+          --w.idx;
+          mbar_wait(&full[w.idx], w.ph, P.err);
+        }
       }
     }
   } else if (warp == 1) {
     // ---- MMA issuer ----
     if (lane == 0) {
-      uint32_t g = 0;
+      Ring rs, ra;
       int local = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
-        const TcItem item = P.items[it];
-        const uint32_t N = (uint32_t)((item.n + 15) / 16) * 16;
+        const int ci = it / MS;
+        const TcChunk ch = P.chunks[ci];
+        const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
         const uint32_t idesc = idesc_f16(128, N);
         if (local > 0) {
-          if (!mbar_wait(accempty, (local - 1) & 1, P.err)) {
+          if (!mbar_wait(accempty, (uint32_t)(local - 1) & 1u, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        for (int c = 0; c < kc_per; ++c, ++g) {
-          const int st = g % NS;
-          const int as = g % kAStages;
-          if (!mbar_wait(&full[st], (g / NS) & 1, P.err) || !mbar_wait(&afull[as], (g / kAStages) & 1, P.err)) {
+        for (int c = 0; c < kc_per; ++c) {
+          if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&afull[ra.idx], ra.ph, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bsm = smem_u32(smem + (size_t)st * kStage + kRawSlot);
+          const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kRawSlot);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk)
-            mma_f16_ts(tmem + acc_col, tmem + as * 32 + kk * 8, desc_sw128(bsm + kk * 32), idesc,
-                       (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&empty[st]);
-          mma_commit(&aempty[as]);
+            mma_f16_ts(tmem + acc_col, tmem + ra.idx * kACols + kk * 8,
+                       desc_sw128(bsm + (kk >> 2) * kBSub + (kk & 3) * 32), idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[rs.idx]);
+          mma_commit(&aempty[ra.idx]);
+          rs.next(NS);
+          ra.next(kAStages);
         }
         if (ok) mma_commit(accfull);
       }
-      if (!ok) s_fail = 1;
       // drain: every MMA this thread issued has completed before TMEM is released
       mma_commit(drain);
       mbar_wait(drain, 0, P.err);
@@ -211,56 +248,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- dequantisation + epilogue ----
     const int dw = warp - 2;
     const int q = warp & 3;        // TMEM lane quarter of this warp
-    const int half = dw >> 2;      // which 32-element half of a 64-element chunk (and of N)
+    const int half = dw >> 2;      // which 64-element half of a 128-element stage (and of N)
     const int r = 32 * q + lane;   // tile row owned by this thread
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    uint32_t g = 0;
+    const int code_off0 = ((2 * half) * 128 + r) * 16;
+    const int code_off1 = ((2 * half + 1) * 128 + r) * 16;
+    const int scale_off = kCodeBytes + r * 8 + half * 4;
+    Ring rs, ra;
     int local = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
-      const TcItem item = P.items[it];
-      for (int c = 0; c < kc_per; ++c, ++g) {
-        const int st = g % NS;
-        const int as = g % kAStages;
-        if (!mbar_wait(&full[st], (g / NS) & 1, P.err) || !mbar_wait(&aempty[as], ((g / kAStages) & 1) ^ 1, P.err)) {
+      for (int c = 0; c < kc_per; ++c) {
+        if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&aempty[ra.idx], ra.ph ^ 1u, P.err)) {
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + (size_t)st * kStage;
-        const uint4 cw = *reinterpret_cast<const uint4*>(raw + (half * 128 + r) * 16);
-        const uint16_t sw = *reinterpret_cast<const uint16_t*>(raw + 4096 + r * 4 + half * 2);
+        const uint8_t* raw = smem + (size_t)rs.idx * kStage;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(raw + code_off0);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(raw + code_off1);
+        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        const uint32_t s2 = e4m3x2_to_f16x2(sw);
-        const uint32_t sa = prmt(s2, s2, 0x1010u);  // (scale of block 0, same)
-        const uint32_t sb = prmt(s2, s2, 0x3232u);  // (scale of block 1, same)
-        uint32_t v[16];
-        e2m1x8_to_f16x2x4(cw.x, v[0], v[1], v[2], v[3]);
-        e2m1x8_to_f16x2x4(cw.y, v[4], v[5], v[6], v[7]);
-        e2m1x8_to_f16x2x4(cw.z, v[8], v[9], v[10], v[11]);
-        e2m1x8_to_f16x2x4(cw.w, v[12], v[13], v[14], v[15]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], sa);
-#pragma unroll
-        for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], sb);
+        if (lane == 0) mbar_arrive(&empty[rs.idx]);
+        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
+        const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
+        uint32_t v[32];
+        dequant_unit(c0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
+        dequant_unit(c1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
         __syncwarp();
-        tmem_st16(tmem + lane_base + (uint32_t)(as * 32 + half * 16), v);
+        tmem_st32(tmem + lane_base + (uint32_t)(ra.idx * kACols + half * 32), v);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[as]);
+        if (lane == 0) mbar_arrive(&afull[ra.idx]);
+        rs.next(NS);
+        ra.next(kAStages);
       }
       if (!ok) break;
       // ---- epilogue ----
-      if (!mbar_wait(accfull, local & 1, P.err)) {
+      if (!mbar_wait(accfull, (uint32_t)local & 1u, P.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int N = ((item.n + 15) / 16) * 16;
-      const int m = item.ms >> 8, s = item.ms & 0xFF;
+      const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
+      const TcChunk ch = P.chunks[ci];
+      const int N = ((ch.n + 15) / 16) * 16;
       const int c_lo = half * (N / 2), c_hi = c_lo + N / 2;
-      const float gsc = P.gscale[item.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
+      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
       for (int c0 = c_lo; c0 < c_hi; c0 += 8) {
         uint32_t v[8];
         __syncwarp();
@@ -269,23 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int n = c0 + i;
-          const int p = item.p0 + n;
+          const int p = ch.p0 + n;
           const float acc = __uint_as_float(v[i]);
           if (P.mode == kTcModeSwiglu) {
             // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
             const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
             const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
-            if (n < item.n && (r & 1) == 0) {
-              const float rs = P.row_scale[p];
-              const float gv = acc * gsc * rs;
-              const float uv = other * o_gsc * rs;
+            if (n < ch.n && (r & 1) == 0) {
+              const float rsc = P.row_scale[p];
+              const float gv = acc * gsc * rsc;
+              const float uv = other * o_gsc * rsc;
               const float hv = gv / (1.f + expf(-gv)) * uv * kHScaleInv;
               const int f = m * 64 + (r >> 1);
               P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
             }
-          } else if (n < item.n) {
-            const float rs = P.row_scale ? P.row_scale[p] : 1.f;
-            P.out[(size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rs;
+          } else if (n < ch.n) {
+            const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
+            P.out[(size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
           }
         }
       }
@@ -293,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty);
     }
-    if (!ok) s_fail = 1;
   }
   tc_fence_before();
   __syncthreads();
@@ -348,73 +381,6 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
       o[j] = *reinterpret_cast<const uint32_t*>(&hh);
     }
     dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-// ---- work list ---------------------------------------------------------------------------
-
-// One thread per touched expert: its rows are cut into chunks of at most nmax and
-// every (chunk, M tile, K split) becomes an item, expert-major so that items
-// sharing an activation tile run close together.
-__global__ void __launch_bounds__(1024) worklist_kernel(const int32_t* __restrict__ active,
-                                                        const int32_t* __restrict__ meta,
-                                                        const int32_t* __restrict__ offsets, int nmax, int M1, int S1,
-                                                        TcItem* __restrict__ items1, int32_t* __restrict__ n1, int cap1,
-                                                        int M2, int S2, TcItem* __restrict__ items2,
-                                                        int32_t* __restrict__ n2, int cap2, uint32_t* err) {
-  __shared__ int warp_sums[32];
-  __shared__ int totals[2];
-  const int a = threadIdx.x;
-  const int nact = meta[0];
-  int e = 0, p0 = 0, ne = 0, nch = 0;
-  if (a < nact) {
-    e = active[a];
-    p0 = offsets[e];
-    ne = offsets[e + 1] - p0;
-    nch = (ne + nmax - 1) / nmax;
-  }
-  int base[2];
-  const int cnt[2] = {nch * M1 * S1, nch * M2 * S2};
-  for (int which = 0; which < 2; ++which) {
-    // block-wide exclusive scan of cnt[which]
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int incl = cnt[which];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_sums[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      const int ws = warp_sums[lane];
-      int wi = ws;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
-        if (lane >= off) wi += o;
-      }
-      warp_sums[lane] = wi - ws;
-      if (lane == 31) totals[which] = wi;
-    }
-    __syncthreads();
-    base[which] = warp_sums[wid] + incl - cnt[which];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const int t1 = totals[0], t2 = totals[1];
-    if (t1 > cap1 || t2 > cap2) atomicOr(err, kErrCountOverflow);
-    *n1 = min(t1, cap1);
-    *n2 = min(t2, cap2);
-  }
-  for (int which = 0; which < 2; ++which) {
-    const int M = which ? M2 : M1, S = which ? S2 : S1, cap = which ? cap2 : cap1;
-    TcItem* items = which ? items2 : items1;
-    int idx = base[which];
-    for (int ch = 0; ch < nch; ++ch)
-      for (int m = 0; m < M; ++m)
-        for (int s = 0; s < S; ++s, ++idx)
-          if (idx < cap) items[idx] = TcItem{e, p0 + ch * nmax, min(nmax, ne - ch * nmax), (m << 8) | s};
   }
 }
 
@@ -491,31 +457,30 @@ cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& 
 
 // ---- load-time repack into the tensor-core tile layout ------------------------------------------
 
-// Tile layout: [M tiles][K chunks of 64][4608 B]: codes as [half (2)][row (128)][16 B],
-// then scales as [row (128)][4 B]. Gate/up tiles interleave rows: tile row 2i is gate
-// feature 64m+i, row 2i+1 is up feature 64m+i. Down tiles: row r is output 128m+r.
+// Tile layout: [M tiles][K chunks of 128][9216 B]: codes as [unit (4)][row (128)][16 B]
+// (unit u = elements 32u..32u+31 of the chunk), then scales as [row (128)][8 B].
+// Gate/up tiles interleave rows: tile row 2i is gate feature 64m+i, row 2i+1 is up
+// feature 64m+i. Down tiles: row r is output feature 128m+r.
 __global__ void repack_tc_kernel(const uint8_t* __restrict__ raw_c, const uint8_t* __restrict__ raw_s,
-                                 uint8_t* __restrict__ out, int rows_total, int K, int M, int gateup, int half_rows) {
-  const int KC = K / 64;
-  const size_t units = (size_t)M * KC * (2 * 128 + 128);  // 16-byte code units + 4-byte scale units
+                                 uint8_t* __restrict__ out, int K, int M, int gateup, int half_rows) {
+  const int KC = K / kChunkK;
+  const size_t units = (size_t)M * KC * 640;  // 512 code units of 16 B + 128 scale units of 8 B per tile
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units) return;
-  const size_t tile = i / (384);
-  const int u = (int)(i % 384);
+  const size_t tile = i / 640;
+  const int u = (int)(i % 640);
   const int m = (int)(tile / KC), kc = (int)(tile % KC);
   uint8_t* dst = out + tile * kRawBytes;
-  if (u < 256) {
-    const int hf = u / 128, r = u % 128;
-    const int R = gateup ? ((r & 1) ? half_rows + m * 64 + (r >> 1) : m * 64 + (r >> 1)) : m * 128 + r;
-    *reinterpret_cast<uint4*>(dst + (hf * 128 + r) * 16) =
-        *reinterpret_cast<const uint4*>(raw_c + (size_t)R * (K / 2) + kc * 32 + hf * 16);
+  const int r = (u < 512) ? (u % 128) : (u - 512);
+  const int R = gateup ? ((r & 1) ? half_rows + m * 64 + (r >> 1) : m * 64 + (r >> 1)) : m * 128 + r;
+  if (u < 512) {
+    const int unit = u / 128;
+    *reinterpret_cast<uint4*>(dst + (unit * 128 + r) * 16) =
+        *reinterpret_cast<const uint4*>(raw_c + (size_t)R * (K / 2) + kc * 64 + unit * 16);
   } else {
-    const int r = u - 256;
-    const int R = gateup ? ((r & 1) ? half_rows + m * 64 + (r >> 1) : m * 64 + (r >> 1)) : m * 128 + r;
-    *reinterpret_cast<uint32_t*>(dst + 4096 + r * 4) =
-        *reinterpret_cast<const uint32_t*>(raw_s + (size_t)R * (K / 16) + kc * 4);
+    *reinterpret_cast<uint2*>(dst + kCodeBytes + r * 8) =
+        *reinterpret_cast<const uint2*>(raw_s + (size_t)R * (K / 16) + kc * 8);
   }
-  (void)rows_total;
 }
 
 cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
@@ -523,12 +488,12 @@ cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw
                              cudaStream_t s) {
   const int H = sh.H, I = sh.I;
   const int M1 = 2 * I / 128, M2 = H / 128;
-  const size_t per1 = (size_t)M1 * (H / 64) * kRawBytes, per2 = (size_t)M2 * (I / 64) * kRawBytes;
-  const size_t u1 = (size_t)M1 * (H / 64) * 384, u2 = (size_t)M2 * (I / 64) * 384;
-  repack_tc_kernel<<<(unsigned)((u1 + 255) / 256), 256, 0, s>>>(gu_codes_raw, gu_scales_raw, gu_tc + e * per1, 2 * I,
-                                                                H, M1, 1, I);
-  repack_tc_kernel<<<(unsigned)((u2 + 255) / 256), 256, 0, s>>>(dn_codes_raw, dn_scales_raw, dn_tc + e * per2, H, I,
-                                                                M2, 0, 0);
+  const size_t per1 = (size_t)M1 * (H / kChunkK) * kRawBytes, per2 = (size_t)M2 * (I / kChunkK) * kRawBytes;
+  const size_t u1 = (size_t)M1 * (H / kChunkK) * 640, u2 = (size_t)M2 * (I / kChunkK) * 640;
+  repack_tc_kernel<<<(unsigned)((u1 + 255) / 256), 256, 0, s>>>(gu_codes_raw, gu_scales_raw, gu_tc + e * per1, H, M1,
+                                                                1, I);
+  repack_tc_kernel<<<(unsigned)((u2 + 255) / 256), 256, 0, s>>>(dn_codes_raw, dn_scales_raw, dn_tc + e * per2, I, M2,
+                                                                0, 0);
   return cudaGetLastError();
 }
 
@@ -541,14 +506,14 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   pl.nmax = pl.prefill ? kTcPrefillN : kTcDecodeN;
   pl.ctas_per_sm = pl.prefill ? 1 : 2;
   pl.grid = sm_count * pl.ctas_per_sm;
-  const int M1 = 2 * sh.I / 128, M2 = sh.H / 128, KC1 = sh.H / 64, KC2 = sh.I / 64;
+  const int M1 = 2 * sh.I / 128, M2 = sh.H / 128, KC1 = sh.H / kChunkK, KC2 = sh.I / kChunkK;
   // expected touched experts for uniform routing
   const double d = sh.E * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
   const double target = 4.0 * pl.grid;
   auto pick = [&](double items, int KC) {
     int want = (int)ceil(target / (items > 1 ? items : 1));
     int best = 1;
-    for (int s = 1; s <= KC / 4 && s <= 64; ++s)
+    for (int s = 1; s <= KC / 3 && s <= 64; ++s)
       if (KC % s == 0 && s <= want) best = s;
     return best;
   };
@@ -557,23 +522,15 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   return pl;
 }
 
-size_t tc_items_cap(const Shape& sh, int T, int which, int sm_count) {
+size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
   const TcPlan pl = tc_plan(sh, T, sm_count);
   const size_t rows = (size_t)T * sh.k;
-  const size_t chunks = (size_t)std::min<size_t>(sh.E, rows) + rows / pl.nmax + 1;
-  const int M = which == 1 ? 2 * sh.I / 128 : sh.H / 128;
-  return chunks * M * (which == 1 ? pl.S1 : pl.S2);
+  return (size_t)std::min<size_t>(sh.E, rows) + rows / pl.nmax + 1;
 }
 
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s) {
   const int rows = T * sh.k;
   gather_x_f16_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_worklist(const Shape& sh, const Workspace& ws, const TcPlan& pl, cudaStream_t s) {
-  worklist_kernel<<<1, 1024, 0, s>>>(ws.active, ws.meta, ws.offsets, pl.nmax, 2 * sh.I / 128, pl.S1, ws.items1,
-                                     ws.n_items1, ws.cap1, sh.H / 128, pl.S2, ws.items2, ws.n_items2, ws.cap2, ws.err);
   return cudaGetLastError();
 }
 

@@ -60,17 +60,19 @@ struct DeviceLayer {
 constexpr float kHScaleInv = 1.0f / 256.0f;
 constexpr float kHScale = 256.0f;
 constexpr int kTcDecodeN = 32;        // rows per work item, decode variant
-constexpr int kTcDecodeStages = 10;   // pipeline stages, decode variant (2 CTAs per SM)
-constexpr int kTcPrefillN = 256;      // rows per work item, prefill variant
-constexpr int kTcPrefillStages = 4;   // pipeline stages, prefill variant (1 CTA per SM)
+constexpr int kTcDecodeStages = 5;    // pipeline stages, decode variant (2 CTAs per SM)
+constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
+constexpr int kTcPrefillStages = 3;   // pipeline stages, prefill variant (1 CTA per SM)
 constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums
 constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes f16 h
 
-struct TcItem {
+// A run of at most nmax routed rows of one expert; every (chunk, M tile, K split)
+// is one work item of the grouped GEMM, decoded arithmetically from its index.
+struct TcChunk {
   int e;   // expert
   int p0;  // first routed row
-  int n;   // rows (<= NMAX)
-  int ms;  // (M tile << 8) | K split
+  int n;   // rows (<= nmax)
+  int pad;
 };
 
 struct TcPlan {
@@ -84,8 +86,8 @@ struct TcPlan {
 struct TcGemmParams {
   const uint8_t* w = nullptr;        // tile-layout weights [E][M][KC][4608]
   int M = 0, KC = 0, S = 1;
-  const TcItem* items = nullptr;
-  const int32_t* n_items = nullptr;
+  const TcChunk* chunks = nullptr;
+  const int32_t* n_chunks = nullptr;
   const float* gscale = nullptr;     // tensor scales
   int gstride = 1, gsel = 0;         // gscale[e*gstride + (gsel ? row&1 : 0)]
   const float* row_scale = nullptr;  // per routed row, or null
@@ -109,7 +111,7 @@ struct Workspace {
   int32_t* counts = nullptr;      // [E]
   int32_t* offsets = nullptr;     // [E+1]
   int32_t* active = nullptr;      // [E] touched experts, ascending
-  int32_t* meta = nullptr;        // [4]: [0] number of touched experts, [1] max rows per expert
+  int32_t* meta = nullptr;        // [4]: [0] touched experts, [1] max rows per expert, [2] row chunks
   int32_t* perm = nullptr;        // [T*k]
   int32_t* slot = nullptr;        // [T*k]
   int32_t* inv = nullptr;         // [T*k]
@@ -124,11 +126,8 @@ struct Workspace {
   uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations (x 2^-8)
   float* part1 = nullptr;         // [S1][T*k][2I] gate/up partial sums (split K only)
   float* ytc = nullptr;           // [S2][T*k][H] down-projection partial sums
-  TcItem* items1 = nullptr;
-  TcItem* items2 = nullptr;
-  int32_t* n_items1 = nullptr;
-  int32_t* n_items2 = nullptr;
-  int cap1 = 0, cap2 = 0;
+  TcChunk* chunks = nullptr;     // row chunks of the touched experts (count in meta[2])
+  int chunk_cap = 0;
 };
 
 struct Shape {
@@ -144,16 +143,17 @@ size_t router_part_elems(const Shape& sh, int T_max, int sm_count);
 cudaError_t launch_router(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
                           int sm_count, cudaStream_t s);
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s);
-cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s);
+// nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).
+cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
+                           int nmax = 0);
 cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
                                cudaStream_t s);
 cudaError_t launch_down_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
 cudaError_t launch_combine(const Shape& sh, const Workspace& ws, uint16_t* out, int T, cudaStream_t s);
 
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
-size_t tc_items_cap(const Shape& sh, int T, int which, int sm_count);
+size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s);
-cudaError_t launch_worklist(const Shape& sh, const Workspace& ws, const TcPlan& pl, cudaStream_t s);
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const TcGemmParams& P, cudaStream_t s);
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,

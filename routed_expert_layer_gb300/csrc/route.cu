@@ -244,8 +244,10 @@ __device__ int block_exclusive_scan(int v, int* total) {
 __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restrict__ masks,
                                                          int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ active,
-                                                         int32_t* __restrict__ meta, int T, int E) {
-  __shared__ int totals[2];
+                                                         int32_t* __restrict__ meta, int T, int E,
+                                                         TcChunk* __restrict__ chunks, int nmax, int chunk_cap,
+                                                         uint32_t* __restrict__ err) {
+  __shared__ int totals[3];
   __shared__ int max_rows;
   const int e = threadIdx.x;
   const int C = (T + 31) / 32;
@@ -272,6 +274,16 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restr
     meta[0] = totals[1];
     meta[1] = max_rows;
   }
+  if (chunks) {  // the expert's rows cut into runs of at most nmax (uniform branch)
+    const int nch = (run + nmax - 1) / nmax;
+    const int cb = block_exclusive_scan(nch, &totals[2]);
+    for (int j = 0; j < nch; ++j)
+      if (cb + j < chunk_cap) chunks[cb + j] = TcChunk{e, off + j * nmax, min(nmax, run - j * nmax), 0};
+    if (threadIdx.x == 0) {
+      if (totals[2] > chunk_cap) atomicOr(err, kErrCountOverflow);
+      meta[2] = min(totals[2], chunk_cap);
+    }
+  }
 }
 
 // Thread per (t, j): p = offsets[e] + rows of e in earlier chunks + earlier tokens of this chunk.
@@ -295,10 +307,12 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint3
   inv[i] = p;
 }
 
-cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s) {
+cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
+                           int nmax) {
   const int blocks = (T + 255) / 256;
   perm_masks_kernel<<<blocks, 256, 8 * sh.E * sizeof(uint32_t), s>>>(idx, ws.masks, ws.err, T, sh.E, sh.k);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(ws.masks, ws.chunk_base, ws.counts, ws.offsets, ws.active, ws.meta, T, sh.E);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(ws.masks, ws.chunk_base, ws.counts, ws.offsets, ws.active, ws.meta, T, sh.E,
+                                      nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err);
   const int n = T * sh.k;
   perm_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(idx, ws.masks, ws.chunk_base, ws.offsets, ws.perm, ws.slot,
                                                       ws.inv, T, sh.E, sh.k);

@@ -19,7 +19,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libmoe_gb300.so")
-_SOURCES = ["api.cu", "route.cu", "expert_simt.cu", "expert_tc.cu", "noalloc.cu"]
+_SOURCES = ["api.cu", "route.cu", "router_tc.cu", "expert_simt.cu", "expert_tc.cu", "noalloc.cu"]
 _HEADERS = ["moe_internal.cuh", "tc_ptx.cuh"]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

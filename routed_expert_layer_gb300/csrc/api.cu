@@ -27,6 +27,7 @@ struct moe_ctx {
   bool simt = false;     // streaming SIMT expert kernels instead of the tensor-core path
   CUtensorMap tmap_x{};  // f16 activation rows (B of the gate/up GEMM)
   CUtensorMap tmap_h{};  // f16 SwiGLU rows (B of the down GEMM)
+  CUtensorMap tmap_w3{}; // bf16 three-term router weights (A of the router GEMM)
   // profiling
   int prof_max = 0;
   int prof_calls = 0;
@@ -54,8 +55,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// 2D f16 tensor [rows][cols] read in boxes of 64 columns x 16 rows with 128-byte swizzle.
-bool make_tmap_f16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+// 2D 16-bit tensor [rows][cols] read in boxes of 64 columns x box_rows rows with 128-byte swizzle.
+bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool bf16) {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -67,9 +68,10 @@ bool make_tmap_f16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
   }
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+  return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                const_cast<void*>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -101,7 +103,10 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
   char* cur = base;
   Workspace w;
-  w.router_part = carve<float>(cur, router_part_elems(sh, c.max_tokens, sm_count));
+  size_t rpart = router_part_elems(sh, c.max_tokens, sm_count);
+  for (int t = 1; t <= c.max_tokens; ++t)
+    rpart = std::max(rpart, (size_t)router_tc_plan(sh, t, sm_count).S * (size_t)t * E);
+  w.router_part = carve<float>(cur, rpart);
   w.logits = carve<float>(cur, T * E);
   w.idx = carve<int32_t>(cur, T * k);
   w.w = carve<float>(cur, T * k);
@@ -141,7 +146,7 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
 
 size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t** gu_c, uint8_t** gu_s,
                       uint8_t** dn_c, uint8_t** dn_s, float** rw, float** rb, float** gug, float** dng,
-                      uint8_t** gu_tc, uint8_t** dn_tc) {
+                      uint8_t** gu_tc, uint8_t** dn_tc, uint16_t** w3) {
   const size_t E = c.n_experts, H = c.hidden, I = c.inter;
   char* cur = base;
   *rw = carve<float>(cur, H * E);
@@ -154,7 +159,9 @@ size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t**
   *dn_s = carve<uint8_t>(cur, E * H * (I / 16));
   *gu_tc = carve<uint8_t>(cur, E * (2 * I / 128) * (H / 128) * 9216);
   *dn_tc = carve<uint8_t>(cur, E * (H / 128) * (I / 128) * 9216);
+  *w3 = carve<uint16_t>(cur, ((E + 127) / 128) * 128 * 3 * H);
   if (L) {
+    L->router_w3 = *w3;
     L->gu_tc = *gu_tc;
     L->dn_tc = *dn_tc;
     L->router_w = *rw;
@@ -193,7 +200,14 @@ struct StageTimer {
 int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax = 0) {
   cudaError_t e;
   if (tm) tm->begin(kStageRouter);
-  e = launch_router(ctx->sh, ctx->L, ctx->ws, x, T, ctx->sm_count, s);
+  if (ctx->simt) {
+    e = launch_router(ctx->sh, ctx->L, ctx->ws, x, T, ctx->sm_count, s);
+  } else {
+    const RouterTcPlan pl = router_tc_plan(ctx->sh, T, ctx->sm_count);
+    CUtensorMap mx;
+    if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)ctx->sh.H, (uint32_t)pl.nt, true)) return MOE_ERR_CUDA;
+    e = launch_router_tc(ctx->sh, pl, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s);
+  }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageRouter);
   if (tm) tm->begin(kStageSelect);
@@ -354,8 +368,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return MOE_ERR_CUDA;
   }
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
-  if (!make_tmap_f16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden) ||
-      !make_tmap_f16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter)) {
+  if (!make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
+      !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false)) {
     cudaFree(ctx->ws_mem);
     delete ctx;
     return MOE_ERR_CUDA;
@@ -376,10 +390,11 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
     if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   uint8_t *gu_c, *gu_s, *dn_c, *dn_s, *gu_tc, *dn_tc;
+  uint16_t* w3;
   float *rw, *rb, *gug, *dng;
   if (!ctx->weights_mem) {
     ctx->weights_bytes =
-        weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc, &dn_tc);
+        weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc, &dn_tc, &w3);
     if (cudaMalloc(&ctx->weights_mem, ctx->weights_bytes) != cudaSuccess) {
       cudaGetLastError();
       ctx->weights_mem = nullptr;
@@ -388,7 +403,7 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   }
   ctx->loaded = false;
   weights_layout(c, &ctx->L, (char*)ctx->weights_mem, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc,
-                 &dn_tc);
+                 &dn_tc, &w3);
   const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
   uint8_t* staging = nullptr;
   if (cudaMalloc(&staging, gu_cb + gu_sb + dn_cb + dn_sb) != cudaSuccess) {
@@ -407,6 +422,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
       if (cudaMemcpy(rb, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
     } else if (cudaMemset(rb, 0, E * sizeof(float)) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
     if (cudaMemcpy(gug, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    if (launch_router_split(ctx->sh, rw, w3, s) != cudaSuccess ||
+        !make_tmap_16(&ctx->tmap_w3, w3, ((E + 127) / 128) * 128, 3 * H, 128, true)) { st = MOE_ERR_CUDA; break; }
     if (cudaMemcpy(dng, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
     for (size_t e = 0; e < E && st == MOE_OK; ++e) {
       if (cudaStreamSynchronize(s) != cudaSuccess) { st = MOE_ERR_CUDA; break; }

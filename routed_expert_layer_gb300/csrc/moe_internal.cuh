@@ -42,6 +42,7 @@ constexpr int kRouterTE = 128;    // router tile: experts (one per thread)
 //   64-element K chunk the 32 rows' 4 scale bytes are contiguous (128 B).
 //   down: tile rt covers output rows 32rt..32rt+31, same chunking along K = I.
 struct DeviceLayer {
+  const uint16_t* router_w3 = nullptr; // [E_pad][3H] bf16: three-term split of W_r, transposed
   const uint8_t* gu_tc = nullptr;     // [E][2I/128][H/64][4608] tensor-core tile layout
   const uint8_t* dn_tc = nullptr;     // [E][H/128][I/64][4608]
   const float* router_w = nullptr;    // [H][E]
@@ -101,6 +102,22 @@ struct TcGemmParams {
   uint32_t* err = nullptr;
 };
 
+struct RouterTcPlan {
+  int nt = 16;        // tokens per N tile
+  int n_tiles = 1, m_tiles = 1;
+  int kc_total = 0;   // K stages of 64 over the 3H concatenated terms
+  int S = 1;          // K splits
+  int grid = 1;
+  bool small = true;  // N tile <= 64 (deeper pipeline variant)
+};
+
+struct RouterTcParams {
+  int T = 0, E = 0, H = 0;
+  int nt = 16, n_tiles = 1, m_tiles = 1, kc_total = 0, S = 1;
+  float* part = nullptr;  // [S][T][E]
+  uint32_t* err = nullptr;
+};
+
 struct Workspace {
   float* router_part = nullptr;   // [S][T][E]
   float* logits = nullptr;        // [T][E]
@@ -142,6 +159,12 @@ size_t router_part_elems(const Shape& sh, int T_max, int sm_count);
 
 cudaError_t launch_router(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
                           int sm_count, cudaStream_t s);
+cudaError_t launch_router_reduce(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S,
+                                 cudaStream_t s);
+RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count);
+cudaError_t launch_router_split(const Shape& sh, const float* W, uint16_t* w3, cudaStream_t s);
+cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx,
+                             const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s);
 // nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,

@@ -102,6 +102,14 @@ __global__ void router_reduce_kernel(const float* __restrict__ part, const float
   logits[i] = acc + bias[i % E];
 }
 
+cudaError_t launch_router_reduce(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S,
+                                 cudaStream_t s) {
+  const size_t n = (size_t)T * sh.E;
+  router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.router_part, L.router_bias, ws.logits, T, sh.E,
+                                                                    S);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
                           int sm_count, cudaStream_t s) {
   const int S = router_splits(sh, T, sm_count);

@@ -61,6 +61,7 @@ template <int NMAX, int NS>
 constexpr size_t gemm_smem_bytes() {
   return 1024 /*alignment slack*/ + (size_t)NS * (kRawSlot + 2 * NMAX * 128) + 256 /*barriers*/;
 }
+static_assert(kAStages * kACols + 2 * kTcDecodeN <= 256, "two decode CTAs per SM must fit in TMEM");
 
 __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* h) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
@@ -116,22 +117,27 @@ struct Ring {  // stage index and phase parity of a circular buffer of n slots
 
 }  // namespace
 
-// Grouped GEMM over the work items (chunk, M tile, K split). See the file comment.
+// Grouped GEMM over the work items (chunk, M tile, K split), decode variant. Warps:
+// 0 TMA, 1 MMA, 2..9 dequantisation, 10..13 epilogue. Two accumulators in TMEM let
+// the MMA start the next item while the epilogue warps drain the previous one.
+constexpr int kEpiWarps = 4;
+constexpr int kThreadsD = (2 + kDequantWarps + kEpiWarps) * 32;
+
 template <int NMAX, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsD, 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const TcGemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   constexpr int kBSub = NMAX * 128;          // one 64-column K half of the activation tile
   constexpr int kStage = kRawSlot + 2 * kBSub;
-  constexpr uint32_t kCols = tmem_cols(NMAX);
+  constexpr uint32_t kCols = tmem_cols(2 * NMAX);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
   uint64_t* afull = empty + NS;
   uint64_t* aempty = afull + kAStages;
-  uint64_t* accfull = aempty + kAStages;
-  uint64_t* accempty = accfull + 1;
-  uint64_t* drain = accempty + 1;
+  uint64_t* accfull = aempty + kAStages;  // [2]
+  uint64_t* accempty = accfull + 2;       // [2]
+  uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&afull[a], kDequantWarps);
       mbar_init(&aempty[a], 1);
     }
-    mbar_init(accfull, 1);
-    mbar_init(accempty, kDequantWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kEpiWarps);
+    }
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -215,13 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TcChunk ch = P.chunks[ci];
         const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
         const uint32_t idesc = idesc_f16(128, N);
-        if (local > 0) {
-          if (!mbar_wait(accempty, (uint32_t)(local - 1) & 1u, P.err)) {
+        const int b = local & 1;
+        if (local >= 2) {  // the epilogue of item local-2 has drained this accumulator
+          if (!mbar_wait(&accempty[b], (uint32_t)((local - 2) >> 1) & 1u, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
+        const uint32_t acc = tmem + acc_col + b * NMAX;
         for (int c = 0; c < kc_per; ++c) {
           if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&afull[ra.idx], ra.ph, P.err)) {
             ok = false;
@@ -231,33 +241,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kRawSlot);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk)
-            mma_f16_ts(tmem + acc_col, tmem + ra.idx * kACols + kk * 8,
-                       desc_sw128(bsm + (kk >> 2) * kBSub + (kk & 3) * 32), idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(acc, tmem + ra.idx * kACols + kk * 8, desc_sw128(bsm + (kk >> 2) * kBSub + (kk & 3) * 32),
+                       idesc, (c > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[rs.idx]);
           mma_commit(&aempty[ra.idx]);
           rs.next(NS);
           ra.next(kAStages);
         }
-        if (ok) mma_commit(accfull);
+        if (ok) mma_commit(&accfull[b]);
       }
       // drain: every MMA this thread issued has completed before TMEM is released
       mma_commit(drain);
       mbar_wait(drain, 0, P.err);
     }
-  } else {
-    // ---- dequantisation + epilogue ----
+  } else if (warp < 2 + kDequantWarps) {
+    // ---- dequantisation ----
     const int dw = warp - 2;
     const int q = warp & 3;        // TMEM lane quarter of this warp
-    const int half = dw >> 2;      // which 64-element half of a 128-element stage (and of N)
+    const int half = dw >> 2;      // which 64-element half of a 128-element stage
     const int r = 32 * q + lane;   // tile row owned by this thread
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int code_off0 = ((2 * half) * 128 + r) * 16;
     const int code_off1 = ((2 * half + 1) * 128 + r) * 16;
-    const int scale_off = kCodeBytes + r * 8 + half * 4;
+    const int scale_off = kCodeBytes + half * 512 + r * 4;
     Ring rs, ra;
-    int local = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
       for (int c = 0; c < kc_per; ++c) {
         if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&aempty[ra.idx], ra.ph ^ 1u, P.err)) {
           ok = false;
@@ -283,22 +292,255 @@ __global__ void __launch_bounds__(kThreads, 1)
         rs.next(NS);
         ra.next(kAStages);
       }
+    }
+  } else {
+    // ---- epilogue ----
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    int local = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
+      const int b = local & 1;
+      if (!mbar_wait(&accfull[b], (uint32_t)(local >> 1) & 1u, P.err)) break;
+      tc_fence_after();
+      const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
+      const TcChunk ch = P.chunks[ci];
+      const int N = ((ch.n + 15) / 16) * 16;
+      uint32_t v[NMAX];
+#pragma unroll
+      for (int c0 = 0; c0 < NMAX; c0 += 8) {
+        if (c0 < N) {
+          __syncwarp();
+          tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(b * NMAX + c0), *reinterpret_cast<uint32_t(*)[8]>(v + c0));
+        }
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
+#pragma unroll
+      for (int n = 0; n < NMAX; ++n) {
+        if (n >= N) break;
+        const int p = ch.p0 + n;
+        const float acc = __uint_as_float(v[n]);
+        if (P.mode == kTcModeSwiglu) {
+          // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
+          const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+          const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
+          if (n < ch.n && (r & 1) == 0) {
+            const float rsc = P.row_scale[p];
+            const float gv = acc * gsc * rsc;
+            const float uv = other * o_gsc * rsc;
+            const float hv = gv / (1.f + expf(-gv)) * uv * kHScaleInv;
+            const int f = m * 64 + (r >> 1);
+            P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
+          }
+        } else if (n < ch.n) {
+          const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
+          P.out[(size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ---- prefill variant: two weight tiles per activation tile -----------------------------
+
+// Each CTA computes two adjacent 128-row weight tiles (M tiles 2mp and 2mp+1) of one
+// row chunk, so every activation tile staged in shared memory feeds twice the MMA
+// work; stages are 64 elements of K (one 128-byte swizzle row), six deep. TMEM: two
+// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns.
+template <int NMAX, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_mt2_kernel(const __grid_constant__ CUtensorMap tmap_b, const TcGemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  constexpr int kHalfRaw = 4608;              // one tile's 64-element K slice: 4096 B codes + 512 B scales
+  constexpr int kASlot = 10240;               // two tiles' raw slices, padded to 1024
+  constexpr int kStage = kASlot + NMAX * 128;
+  constexpr int kA2 = 2;                      // A stages in TMEM (each 2 tiles x 32 columns)
+  constexpr uint32_t kCols = 512;
+  static_assert(kA2 * 64 + 2 * NMAX <= 512, "TMEM budget");
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
+  uint64_t* empty = full + NS;
+  uint64_t* afull = empty + NS;
+  uint64_t* aempty = afull + kA2;
+  uint64_t* accfull = aempty + kA2;
+  uint64_t* accempty = accfull + 1;
+  uint64_t* drain = accempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDequantWarps + 1);
+    }
+    for (int a = 0; a < kA2; ++a) {
+      mbar_init(&afull[a], kDequantWarps);
+      mbar_init(&aempty[a], 1);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(accempty, kDequantWarps);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t acc_col = kA2 * 64;
+  const int MP = P.M / 2;
+  const int n_items = *P.n_chunks * MP;
+  const int n64 = P.KC * 2;  // 64-element K stages over the whole K (no K split in this variant)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      Ring rs;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const int ci = it / MP, mp = it - ci * MP;
+        const TcChunk ch = P.chunks[ci];
+        const int nb = (ch.n + kBoxRows - 1) / kBoxRows;
+        const uint8_t* w0 = P.w + (size_t)(ch.e * P.M + 2 * mp) * P.KC * kRawBytes;
+        const uint8_t* w1 = w0 + (size_t)P.KC * kRawBytes;
+        const uint32_t tx = 2 * kHalfRaw + nb * kBoxBytes;
+        for (int c = 0; c < n64; ++c) {
+          if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sb = smem + (size_t)rs.idx * kStage;
+          const size_t off = (size_t)(c >> 1) * kRawBytes;
+          const int h = c & 1;
+          mbar_arrive_expect_tx(&full[rs.idx], tx);
+          bulk_g2s(sb, w0 + off + h * 4096, 4096, &full[rs.idx]);
+          bulk_g2s(sb + 4096, w0 + off + kCodeBytes + h * 512, 512, &full[rs.idx]);
+          bulk_g2s(sb + kHalfRaw, w1 + off + h * 4096, 4096, &full[rs.idx]);
+          bulk_g2s(sb + kHalfRaw + 4096, w1 + off + kCodeBytes + h * 512, 512, &full[rs.idx]);
+          for (int b = 0; b < nb; ++b)
+            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
+          ++issued;
+          rs.next(NS);
+        }
+      }
+      if (!ok) {
+        Ring w = rs;
+        for (uint32_t j = 0; j < (issued < (uint32_t)NS ? issued : (uint32_t)NS); ++j) {
+          if (w.idx == 0) {
+            w.idx = NS;
+            w.ph ^= 1u;
+          }
+          --w.idx;
+          mbar_wait(&full[w.idx], w.ph, P.err);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      Ring rs, ra;
+      int local = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
+        const TcChunk ch = P.chunks[it / MP];
+        const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
+        const uint32_t idesc = idesc_f16(128, N);
+        if (local > 0) {
+          if (!mbar_wait(accempty, (uint32_t)(local - 1) & 1u, P.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int c = 0; c < n64; ++c) {
+          if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&afull[ra.idx], ra.ph, P.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kASlot);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts(tmem + acc_col + t * NMAX, tmem + ra.idx * 64 + t * 32 + kk * 8, desc_sw128(bsm + kk * 32),
+                         idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[rs.idx]);
+          mma_commit(&aempty[ra.idx]);
+          rs.next(NS);
+          ra.next(kA2);
+        }
+        if (ok) mma_commit(accfull);
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, P.err);
+    }
+  } else {
+    const int dw = warp - 2;
+    const int q = warp & 3;
+    const int t = dw >> 2;  // which of the two weight tiles this warp serves
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const int code_off0 = t * kHalfRaw + r * 16;
+    const int code_off1 = t * kHalfRaw + (128 + r) * 16;
+    const int scale_off = t * kHalfRaw + 4096 + r * 4;
+    Ring rs, ra;
+    int local = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
+      for (int c = 0; c < n64; ++c) {
+        if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&aempty[ra.idx], ra.ph ^ 1u, P.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = smem + (size_t)rs.idx * kStage;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(raw + code_off0);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(raw + code_off1);
+        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[rs.idx]);
+        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
+        const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
+        uint32_t v[32];
+        dequant_unit(c0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
+        dequant_unit(c1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
+        __syncwarp();
+        tmem_st32(tmem + lane_base + (uint32_t)(ra.idx * 64 + t * 32), v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[ra.idx]);
+        rs.next(NS);
+        ra.next(kA2);
+      }
       if (!ok) break;
-      // ---- epilogue ----
       if (!mbar_wait(accfull, (uint32_t)local & 1u, P.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
+      const int ci = it / MP, mp = it - ci * MP;
+      const int m = 2 * mp + t;
       const TcChunk ch = P.chunks[ci];
       const int N = ((ch.n + 15) / 16) * 16;
-      const int c_lo = half * (N / 2), c_hi = c_lo + N / 2;
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
-      for (int c0 = c_lo; c0 < c_hi; c0 += 8) {
+      for (int c0 = 0; c0 < N; c0 += 8) {
         uint32_t v[8];
         __syncwarp();
-        tmem_ld8(tmem + lane_base + acc_col + (uint32_t)c0, v);
+        tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(t * NMAX + c0), v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -306,7 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int p = ch.p0 + n;
           const float acc = __uint_as_float(v[i]);
           if (P.mode == kTcModeSwiglu) {
-            // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
             const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
             const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
             if (n < ch.n && (r & 1) == 0) {
@@ -319,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if (n < ch.n) {
             const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
-            P.out[(size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
+            P.out[(size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
           }
         }
       }
@@ -458,7 +699,9 @@ cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& 
 // ---- load-time repack into the tensor-core tile layout ------------------------------------------
 
 // Tile layout: [M tiles][K chunks of 128][9216 B]: codes as [unit (4)][row (128)][16 B]
-// (unit u = elements 32u..32u+31 of the chunk), then scales as [row (128)][8 B].
+// (unit u = elements 32u..32u+31 of the chunk), then scales as [half (2)][row (128)][4 B]
+// (half h = the E4M3 scales of elements 64h..64h+63), so each 64-element half of a
+// chunk is two contiguous pieces: codes [4096h, 4096h+4096) and scales [8192+512h, +512).
 // Gate/up tiles interleave rows: tile row 2i is gate feature 64m+i, row 2i+1 is up
 // feature 64m+i. Down tiles: row r is output feature 128m+r.
 __global__ void repack_tc_kernel(const uint8_t* __restrict__ raw_c, const uint8_t* __restrict__ raw_s,
@@ -478,8 +721,9 @@ __global__ void repack_tc_kernel(const uint8_t* __restrict__ raw_c, const uint8_
     *reinterpret_cast<uint4*>(dst + (unit * 128 + r) * 16) =
         *reinterpret_cast<const uint4*>(raw_c + (size_t)R * (K / 2) + kc * 64 + unit * 16);
   } else {
-    *reinterpret_cast<uint2*>(dst + kCodeBytes + r * 8) =
-        *reinterpret_cast<const uint2*>(raw_s + (size_t)R * (K / 16) + kc * 8);
+    const uint2 sc = *reinterpret_cast<const uint2*>(raw_s + (size_t)R * (K / 16) + kc * 8);
+    *reinterpret_cast<uint32_t*>(dst + kCodeBytes + r * 4) = sc.x;        // blocks 0..3 (first 64 of K)
+    *reinterpret_cast<uint32_t*>(dst + kCodeBytes + 512 + r * 4) = sc.y;  // blocks 4..7
   }
 }
 
@@ -540,12 +784,22 @@ static cudaError_t launch_gemm_t(const CUtensorMap& map, const TcGemmParams& P, 
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<NMAX, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<NMAX, NS><<<grid, kThreads, smem, s>>>(map, P);
+  grouped_gemm_kernel<NMAX, NS><<<grid, kThreadsD, smem, s>>>(map, P);
+  return cudaGetLastError();
+}
+
+template <int NMAX, int NS>
+static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
+  const size_t smem = 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<NMAX, NS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreads, smem, s>>>(map, P);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const TcGemmParams& P, cudaStream_t s) {
-  if (pl.prefill) return launch_gemm_t<kTcPrefillN, kTcPrefillStages>(map, P, pl.grid, s);
+  if (pl.prefill) return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages>(map, P, pl.grid, s);
   return launch_gemm_t<kTcDecodeN, kTcDecodeStages>(map, P, pl.grid, s);
 }
 

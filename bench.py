@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--T", type=int, default=53)
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration side measurements")
     ap.add_argument("--cpu-sample", type=int, default=0, help="tokens in the oracle sample (0 = auto)")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only run warmup+steps forwards of a K3-shaped layer with --experts experts "
+                         "(no timing line): the command the ncu captures in profiles/ use")
+    ap.add_argument("--experts", type=int, default=896, help="experts in the layer (--profile-run only)")
     return ap.parse_args()
 
 
@@ -166,25 +170,58 @@ def touched(moe, x_dev, E, k):
 
 
 def time_config(moe, xs, steps, warmup, stream, profile=False):
-    """Device time per forward (CUDA events on the launching stream), rotating batches."""
+    """Device time per forward: each rotating batch's forward is captured once in a CUDA
+    graph and the graphs are replayed in turn; CUDA events on the launching stream bracket
+    the timed replays. Returns (ms per forward, per-stage profile, kernels launched)."""
     import torch
     outs = [torch.empty_like(x) for x in xs]
     with torch.cuda.stream(stream):
+        for i in range(len(xs)):  # eager first pass (lazy module loading, first touch)
+            moe.forward(xs[i], outs[i], stream)
+    torch.cuda.synchronize()
+    if profile:
+        moe.profile_begin(len(xs))  # one set of stage events per captured graph
+    n0 = moe.launch_count()
+    graphs = []
+    for i in range(len(xs)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.forward(xs[i], outs[i], stream)
+        graphs.append(g)
+    per_forward = (moe.launch_count() - n0) / len(xs)
+    with torch.cuda.stream(stream):
         for i in range(warmup):
-            moe.forward(xs[i % len(xs)], outs[i % len(xs)], stream)
+            graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
-        if profile:
-            moe.profile_begin(steps)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n0 = moe.launch_count()
         a.record(stream)
         for i in range(steps):
-            moe.forward(xs[i % len(xs)], outs[i % len(xs)], stream)
+            graphs[i % len(graphs)].replay()
         b.record(stream)
-        n1 = moe.launch_count()
         torch.cuda.synchronize()
     prof = moe.profile_end() if profile else None
-    return a.elapsed_time(b) / steps, prof, n1 - n0
+    del graphs
+    return a.elapsed_time(b) / steps, prof, int(per_forward * steps)
+
+
+def profile_run(args):
+    """Forwards of a K3-shaped layer (H=7168, I=1536, k=16) with --experts experts at --T
+    tokens: a small case of the same kernels for ncu captures."""
+    import torch
+    import synth
+    import routed_expert_layer_gb300 as rel
+    L = synth.layer(K3["H"], K3["I"], args.experts, seed_weights=1, seed_router=2)
+    moe = rel.MoeLayer(K3["H"], K3["I"], args.experts, K3["k"], args.T)
+    moe.load(L)
+    x = torch.from_numpy(synth.x_bf16(3, args.T, K3["H"]).view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    for _ in range(args.warmup + args.steps):
+        moe.forward(x, out)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": True, "experts": args.experts, "T": args.T,
+                      "forwards": args.warmup + args.steps, "device_error": moe.get_error(),
+                      "kernels": moe.launch_count()}), flush=True)
+    moe.close()
 
 
 def main():
@@ -192,6 +229,9 @@ def main():
     rank, world, local = dist_info()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.profile_run:
+        profile_run(args)
         return
     import torch
     import torch.distributed as dist

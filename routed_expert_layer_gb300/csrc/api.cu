@@ -183,15 +183,24 @@ struct StageTimer {
   moe_ctx* ctx;
   cudaStream_t s;
   int call;
+  unsigned flags = cudaEventRecordDefault;
   StageTimer(moe_ctx* c, cudaStream_t st) : ctx(c), s(st), call(-1) {
-    if (ctx->prof_max > 0 && ctx->prof_calls < ctx->prof_max) call = ctx->prof_calls++;
+    if (ctx->prof_max > 0 && ctx->prof_calls < ctx->prof_max) {
+      call = ctx->prof_calls++;
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        flags = cudaEventRecordExternal;
+    }
   }
+  // External records so that, under stream capture, the events become event-record
+  // nodes of the graph and every replay times the stage.
   void begin(int stage) {
-    if (call >= 0) cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s);
+    if (call >= 0)
+      cudaEventRecordWithFlags(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s, flags);
   }
   void end(int stage) {
     if (call >= 0) {
-      cudaEventRecord(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 1], s);
+      cudaEventRecordWithFlags(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 1], s, flags);
       ctx->prof_rec[(size_t)call * kNumStages + stage] = 1;
     }
   }
@@ -370,6 +379,13 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
   if (!make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
       !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false)) {
+    cudaFree(ctx->ws_mem);
+    delete ctx;
+    return MOE_ERR_CUDA;
+  }
+  if (tc_configure() != cudaSuccess || router_tc_configure() != cudaSuccess ||
+      simt_configure(ctx->sh) != cudaSuccess) {
+    cudaGetLastError();
     cudaFree(ctx->ws_mem);
     delete ctx;
     return MOE_ERR_CUDA;

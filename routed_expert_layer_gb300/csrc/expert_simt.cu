@@ -232,12 +232,18 @@ __global__ void __launch_bounds__(256) down_simt_kernel(DeviceLayer L, Shape sh,
   }
 }
 
+cudaError_t simt_configure(const Shape& sh) {
+  const size_t s1 = (size_t)kSimtNT * sh.H * sizeof(float) + (size_t)kSimtWarps * 32 * kSimtNT * sizeof(float);
+  const size_t s2 = (size_t)kSimtNT * sh.I * sizeof(float) + (size_t)kSimtWarps * 32 * kSimtNT * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(gateup_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(down_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+}
+
 cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
                                cudaStream_t s) {
   const int slots = min(sh.E, T * sh.k);
   const size_t smem = (size_t)kSimtNT * sh.H * sizeof(float) + (size_t)kSimtWarps * 32 * kSimtNT * sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(gateup_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   dim3 grid(sh.I / 16, slots);
   gateup_simt_kernel<<<grid, 256, smem, s>>>(L, sh, x, ws.active, ws.meta, ws.offsets, ws.perm, ws.h);
   return cudaGetLastError();
@@ -246,8 +252,6 @@ cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Work
 cudaError_t launch_down_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s) {
   const int slots = min(sh.E, T * sh.k);
   const size_t smem = (size_t)kSimtNT * sh.I * sizeof(float) + (size_t)kSimtWarps * 32 * kSimtNT * sizeof(float);
-  cudaError_t err = cudaFuncSetAttribute(down_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
   dim3 grid(sh.H / 32, slots);
   down_simt_kernel<<<grid, 256, smem, s>>>(L, sh, ws.active, ws.meta, ws.offsets, ws.h, ws.y);
   return cudaGetLastError();

@@ -781,20 +781,30 @@ cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t
 template <int NMAX, int NS>
 static cudaError_t launch_gemm_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
   const size_t smem = gemm_smem_bytes<NMAX, NS>();
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<NMAX, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
   grouped_gemm_kernel<NMAX, NS><<<grid, kThreadsD, smem, s>>>(map, P);
   return cudaGetLastError();
 }
 
 template <int NMAX, int NS>
-static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
-  const size_t smem = 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<NMAX, NS>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+constexpr size_t smem_mt2() {
+  return 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;
+}
+
+// Opt the GEMM kernels into large dynamic shared memory (once, at context creation,
+// outside any stream capture).
+cudaError_t tc_configure() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kTcDecodeN, kTcDecodeStages>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemm_smem_bytes<kTcDecodeN, kTcDecodeStages>());
   if (e != cudaSuccess) return e;
-  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreads, smem, s>>>(map, P);
+  return cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcPrefillN, kTcPrefillStages>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_mt2<kTcPrefillN, kTcPrefillStages>());
+}
+
+template <int NMAX, int NS>
+static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
+  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreads, smem_mt2<NMAX, NS>(), s>>>(map, P);
   return cudaGetLastError();
 }
 

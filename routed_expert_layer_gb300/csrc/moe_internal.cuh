@@ -174,6 +174,11 @@ cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Work
 cudaError_t launch_down_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
 cudaError_t launch_combine(const Shape& sh, const Workspace& ws, uint16_t* out, int T, cudaStream_t s);
 
+// Large-shared-memory opt-in for the kernels that need it (call once per context).
+cudaError_t tc_configure();
+cudaError_t router_tc_configure();
+cudaError_t simt_configure(const Shape& sh);
+
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s);

@@ -251,13 +251,18 @@ cudaError_t launch_router_split(const Shape& sh, const float* W, uint16_t* w3, c
   return cudaGetLastError();
 }
 
+cudaError_t router_tc_configure() {
+  cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)router_smem_bytes<64>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(router_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)router_smem_bytes<256>());
+}
+
 template <int NMAX>
 static cudaError_t launch_router_tc_t(const CUtensorMap& mw, const CUtensorMap& mx, const RouterTcParams& P, int grid,
                                       cudaStream_t s) {
-  const size_t smem = router_smem_bytes<NMAX>();
-  cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  router_tc_kernel<NMAX><<<grid, kRThreads, smem, s>>>(mw, mx, P);
+  router_tc_kernel<NMAX><<<grid, kRThreads, router_smem_bytes<NMAX>(), s>>>(mw, mx, P);
   return cudaGetLastError();
 }
 

@@ -172,3 +172,47 @@ def test_profile_hooks(tiny):
         tiny.forward(x, out)
     prof = tiny.profile_end()
     assert prof["gateup"][1] == 3 and prof["gateup"][0] > 0
+
+
+def test_forward_in_cuda_graph(mid):
+    """moe_forward allocates nothing and never syncs the host, so it can be captured in
+    a CUDA graph; replays give exactly the eager result."""
+    import torch
+    x = torch.from_numpy(synth.x_bf16(321, 37, 512).view(np.int16)).cuda()
+    eager = torch.empty_like(x)
+    mid.forward(x, eager)
+    s = torch.cuda.Stream()
+    out = torch.zeros_like(x)
+    with torch.cuda.stream(s):
+        mid.forward(x, out, s)  # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mid.forward(x, out, s)
+    out.zero_()
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    assert mid.get_error() == 0
+
+
+def test_profile_hooks_under_graph_capture(mid):
+    import torch
+    x = torch.from_numpy(synth.x_bf16(77, 37, 512).view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        mid.forward(x, out, s)
+    torch.cuda.synchronize()
+    mid.profile_begin(1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mid.forward(x, out, s)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    prof = mid.profile_end()
+    assert prof["gateup"][1] == 1 and prof["gateup"][0] > 0 and prof["down"][0] > 0

@@ -19,7 +19,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libmoe_gb300.so")
-_SOURCES = ["api.cu", "route.cu", "router_tc.cu", "expert_simt.cu", "expert_tc.cu", "noalloc.cu"]
+_SOURCES = ["api.cu", "route.cu", "router_tc.cu", "expert_tc.cu", "noalloc.cu"]
 _HEADERS = ["moe_internal.cuh", "tc_ptx.cuh"]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -35,8 +35,8 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
-KERNEL_REV = {"router": "simt-1", "select": "warp-1", "permute": "mask-1", "gateup": "simt-1", "down": "simt-1",
-              "combine": "f32-1"}
+KERNEL_REV = {"router": "tc3-1", "select": "warp-1", "permute": "mask-2", "gather": "f16-1",
+              "gateup": "tc-5", "down": "tc-5", "combine": "f32-2"}
 
 
 def _nvcc() -> str:

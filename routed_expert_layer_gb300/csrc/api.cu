@@ -1,5 +1,15 @@
 // C ABI: context, weight loading, the forward launch sequence, inspection hooks.
 // The operations and their sources are documented in include/moe_gb300.h.
+//
+// Forward sequence (all on the caller's stream, no host synchronisation, no
+// allocation, so it can be captured in a CUDA graph):
+//   router_tc (+ reduce)  S1 logits            route.cu / router_tc.cu
+//   select                S2 top-k, weights    route.cu
+//   permute (3 kernels)   S3 offsets, perm, row chunks
+//   gather                f16 activation rows in routed order
+//   gate/up GEMM          S4 (+ K-split reduction with SwiGLU when split)
+//   down GEMM             S5
+//   combine               S6
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -23,16 +33,15 @@ struct moe_ctx {
   size_t weights_bytes = 0;
   void* ws_mem = nullptr;
   size_t ws_bytes = 0;
-  int64_t launches = 0;  // kernels enqueued by forward calls
-  bool simt = false;     // streaming SIMT expert kernels instead of the tensor-core path
-  CUtensorMap tmap_x{};  // f16 activation rows (B of the gate/up GEMM)
-  CUtensorMap tmap_h{};  // f16 SwiGLU rows (B of the down GEMM)
-  CUtensorMap tmap_w3{}; // bf16 three-term router weights (A of the router GEMM)
+  int64_t launches = 0;   // kernels enqueued so far
+  CUtensorMap tmap_x{};   // f16 activation rows (B of the gate/up GEMM)
+  CUtensorMap tmap_h{};   // f16 SwiGLU rows (B of the down GEMM)
+  CUtensorMap tmap_w3{};  // bf16 three-term router weights (A of the router GEMM)
   // profiling
   int prof_max = 0;
   int prof_calls = 0;
   std::vector<cudaEvent_t> prof_ev;  // [prof_max][kNumStages][2]
-  std::vector<uint8_t> prof_rec;     // [prof_max][kNumStages]: stage ran in that call
+  std::vector<uint8_t> prof_rec;     // [prof_max][kNumStages]: the stage ran in that call
 };
 
 namespace {
@@ -48,14 +57,14 @@ struct DeviceGuard {
   }
 };
 
-const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep",
-                                       "gateup", "finalize", "down", "combine"};
+const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep", "gateup", "finalize", "down", "combine"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// 2D 16-bit tensor [rows][cols] read in boxes of 64 columns x box_rows rows with 128-byte swizzle.
+// 2D 16-bit tensor [rows][cols] read in boxes of 64 columns x box_rows rows with
+// 128-byte swizzle. Host-only (no GPU work), so it may run during stream capture.
 bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool bf16) {
   static EncodeTiledFn encode = nullptr;
   if (!encode) {
@@ -71,8 +80,8 @@ bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t co
   const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -88,115 +97,102 @@ int check_config(const moe_config* c) {
   return MOE_OK;
 }
 
-// Carve `bytes` from a bump allocator (256-byte aligned).
-template <typename T>
-T* carve(char*& cur, size_t count) {
-  T* p = reinterpret_cast<T*>(cur);
-  size_t bytes = (count * sizeof(T) + 255) & ~(size_t)255;
-  cur += bytes;
-  return p;
-}
+// Bump allocation from one device block (256-byte aligned). With base == nullptr only
+// the offsets are computed (the returned pointers are then never dereferenced).
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += (count * sizeof(T) + 255) & ~(size_t)255;
+    return p;
+  }
+};
 
 size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* base) {
   const size_t T = c.max_tokens, E = c.n_experts, k = c.top_k, H = c.hidden, I = c.inter;
   const size_t C = (T + 31) / 32;
-  Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
-  char* cur = base;
-  Workspace w;
-  size_t rpart = router_part_elems(sh, c.max_tokens, sm_count);
-  for (int t = 1; t <= c.max_tokens; ++t)
-    rpart = std::max(rpart, (size_t)router_tc_plan(sh, t, sm_count).S * (size_t)t * E);
-  w.router_part = carve<float>(cur, rpart);
-  w.logits = carve<float>(cur, T * E);
-  w.idx = carve<int32_t>(cur, T * k);
-  w.w = carve<float>(cur, T * k);
-  w.masks = carve<uint32_t>(cur, C * E);
-  w.chunk_base = carve<int32_t>(cur, C * E);
-  w.counts = carve<int32_t>(cur, E);
-  w.offsets = carve<int32_t>(cur, E + 1);
-  w.active = carve<int32_t>(cur, E);
-  w.meta = carve<int32_t>(cur, 4);
-  w.perm = carve<int32_t>(cur, T * k);
-  w.slot = carve<int32_t>(cur, T * k);
-  w.inv = carve<int32_t>(cur, T * k);
-  w.h = carve<float>(cur, T * k * I);
-  w.x_stage = carve<uint16_t>(cur, T * H);
-  w.out_stage = carve<uint16_t>(cur, T * H);
-  w.err = carve<uint32_t>(cur, 1);
-  // tensor-core path: sizes are the maxima over every T <= max_tokens of its plan
-  size_t part1 = 0, ytc = T * k * H, ccap = 0;
+  const Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
+  // sizes that depend on the per-T plans: the maxima over every T <= max_tokens
+  size_t rpart = 1, part1 = 1, ytc = T * k * H, ccap = 1;
   for (int t = 1; t <= c.max_tokens; ++t) {
-    const TcPlan pl = tc_plan(sh, t, sm_count);
     const size_t rows = (size_t)t * k;
+    rpart = std::max(rpart, (size_t)router_tc_plan(sh, t, sm_count).S * (size_t)t * E);
+    const TcPlan pl = tc_plan(sh, t, sm_count);
     if (pl.S1 > 1) part1 = std::max(part1, (size_t)pl.S1 * rows * 2 * I);
     ytc = std::max(ytc, (size_t)pl.S2 * rows * H);
     ccap = std::max(ccap, tc_chunk_cap(sh, t, sm_count));
   }
-  w.xg = carve<uint16_t>(cur, T * k * H);
-  w.row_scale = carve<float>(cur, T * k);
-  w.h16 = carve<uint16_t>(cur, T * k * I);
-  w.part1 = carve<float>(cur, std::max<size_t>(part1, 1));
-  w.ytc = carve<float>(cur, ytc);
-  w.y = w.ytc;  // the streaming path's y aliases the same buffer
-  w.chunks = carve<TcChunk>(cur, ccap);
+  Carver cv{base};
+  Workspace w;
+  w.router_part = cv.take<float>(rpart);
+  w.logits = cv.take<float>(T * E);
+  w.idx = cv.take<int32_t>(T * k);
+  w.w = cv.take<float>(T * k);
+  w.masks = cv.take<uint32_t>(C * E);
+  w.chunk_base = cv.take<int32_t>(C * E);
+  w.counts = cv.take<int32_t>(E);
+  w.offsets = cv.take<int32_t>(E + 1);
+  w.active = cv.take<int32_t>(E);
+  w.meta = cv.take<int32_t>(4);
+  w.perm = cv.take<int32_t>(T * k);
+  w.slot = cv.take<int32_t>(T * k);
+  w.inv = cv.take<int32_t>(T * k);
+  w.x_stage = cv.take<uint16_t>(T * H);
+  w.out_stage = cv.take<uint16_t>(T * H);
+  w.err = cv.take<uint32_t>(1);
+  w.xg = cv.take<uint16_t>(T * k * H);
+  w.row_scale = cv.take<float>(T * k);
+  w.h16 = cv.take<uint16_t>(T * k * I);
+  w.part1 = cv.take<float>(part1);
+  w.ytc = cv.take<uint16_t>(ytc);
+  w.chunks = cv.take<TcChunk>(ccap);
   w.chunk_cap = (int)ccap;
   if (ws) *ws = w;
-  return (size_t)(cur - base);
+  return cv.off;
 }
 
-size_t weights_layout(const moe_config& c, DeviceLayer* L, char* base, uint8_t** gu_c, uint8_t** gu_s,
-                      uint8_t** dn_c, uint8_t** dn_s, float** rw, float** rb, float** gug, float** dng,
-                      uint8_t** gu_tc, uint8_t** dn_tc, uint16_t** w3) {
+struct WeightPtrs {
+  float *router_w, *router_bias, *gu_global, *dn_global;
+  uint16_t* w3;
+  uint8_t *gu_tc, *dn_tc;
+};
+
+size_t weights_layout(const moe_config& c, WeightPtrs* p, char* base) {
   const size_t E = c.n_experts, H = c.hidden, I = c.inter;
-  char* cur = base;
-  *rw = carve<float>(cur, H * E);
-  *rb = carve<float>(cur, E);
-  *gug = carve<float>(cur, 2 * E);
-  *dng = carve<float>(cur, E);
-  *gu_c = carve<uint8_t>(cur, E * 2 * I * (H / 2));
-  *gu_s = carve<uint8_t>(cur, E * 2 * I * (H / 16));
-  *dn_c = carve<uint8_t>(cur, E * H * (I / 2));
-  *dn_s = carve<uint8_t>(cur, E * H * (I / 16));
-  *gu_tc = carve<uint8_t>(cur, E * (2 * I / 128) * (H / 128) * 9216);
-  *dn_tc = carve<uint8_t>(cur, E * (H / 128) * (I / 128) * 9216);
-  *w3 = carve<uint16_t>(cur, ((E + 127) / 128) * 128 * 3 * H);
-  if (L) {
-    L->router_w3 = *w3;
-    L->gu_tc = *gu_tc;
-    L->dn_tc = *dn_tc;
-    L->router_w = *rw;
-    L->router_bias = *rb;
-    L->gu_global = *gug;
-    L->dn_global = *dng;
-    L->gu_codes = *gu_c;
-    L->gu_scales = *gu_s;
-    L->dn_codes = *dn_c;
-    L->dn_scales = *dn_s;
-  }
-  return (size_t)(cur - base);
+  Carver cv{base};
+  WeightPtrs w;
+  w.router_w = cv.take<float>(H * E);
+  w.router_bias = cv.take<float>(E);
+  w.gu_global = cv.take<float>(2 * E);
+  w.dn_global = cv.take<float>(E);
+  w.w3 = cv.take<uint16_t>(((E + 127) / 128) * 128 * 3 * H);
+  w.gu_tc = cv.take<uint8_t>(E * 2 * I * H * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
+  w.dn_tc = cv.take<uint8_t>(E * H * I * 9 / 16);
+  if (p) *p = w;
+  return cv.off;
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Events bracketing one stage of a profiled forward (no-ops when not armed).
+// Events bracketing each stage of a profiled forward (no-ops when not armed).
 struct StageTimer {
   moe_ctx* ctx;
   cudaStream_t s;
-  int call;
+  int call = -1;
   unsigned flags = cudaEventRecordDefault;
-  StageTimer(moe_ctx* c, cudaStream_t st) : ctx(c), s(st), call(-1) {
+  StageTimer(moe_ctx* c, cudaStream_t st) : ctx(c), s(st) {
     if (ctx->prof_max > 0 && ctx->prof_calls < ctx->prof_max) {
       call = ctx->prof_calls++;
+      // under stream capture, external records become event nodes timed by every replay
       cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
       if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
         flags = cudaEventRecordExternal;
     }
   }
-  // External records so that, under stream capture, the events become event-record
-  // nodes of the graph and every replay times the stage.
   void begin(int stage) {
-    if (call >= 0)
-      cudaEventRecordWithFlags(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s, flags);
+    if (call >= 0) cudaEventRecordWithFlags(ctx->prof_ev[((size_t)call * kNumStages + stage) * 2 + 0], s, flags);
   }
   void end(int stage) {
     if (call >= 0) {
@@ -206,41 +202,35 @@ struct StageTimer {
   }
 };
 
-int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax = 0) {
-  cudaError_t e;
+// S1..S3. nmax > 0 also emits the row chunks the expert GEMMs iterate over.
+int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax) {
+  const Shape& sh = ctx->sh;
   if (tm) tm->begin(kStageRouter);
-  if (ctx->simt) {
-    e = launch_router(ctx->sh, ctx->L, ctx->ws, x, T, ctx->sm_count, s);
-  } else {
-    const RouterTcPlan pl = router_tc_plan(ctx->sh, T, ctx->sm_count);
-    CUtensorMap mx;
-    if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)ctx->sh.H, (uint32_t)pl.nt, true)) return MOE_ERR_CUDA;
-    e = launch_router_tc(ctx->sh, pl, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s);
-  }
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const RouterTcPlan rp = router_tc_plan(sh, T, ctx->sm_count);
+  CUtensorMap mx;
+  if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)sh.H, (uint32_t)rp.nt, true)) return MOE_ERR_CUDA;
+  if (launch_router_tc(sh, rp, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageRouter);
   if (tm) tm->begin(kStageSelect);
-  e = launch_select(ctx->sh, ctx->ws.logits, ctx->ws.idx, ctx->ws.w, T, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_select(sh, ctx->ws.logits, ctx->ws.idx, ctx->ws.w, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageSelect);
   if (tm) tm->begin(kStagePermute);
-  e = launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s, nmax);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_permute(sh, ctx->ws, ctx->ws.idx, T, s, nmax) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePermute);
   ctx->launches += 6;
   return MOE_OK;
 }
 
-int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, StageTimer* tm,
-                   TcPlan* plan_out) {
+// S4..S6 on the tensor cores, for the plan `pl` (the route must have used pl.nmax).
+int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, const TcPlan& pl,
+                StageTimer* tm) {
   const Shape& sh = ctx->sh;
   const Workspace& ws = ctx->ws;
-  const TcPlan pl = tc_plan(sh, T, ctx->sm_count);
-  if (plan_out) *plan_out = pl;
   const int rows = T * sh.k;
   if (tm) tm->begin(kStagePrep);
   if (launch_gather_x(sh, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePrep);
+
   TcGemmParams P1;
   P1.w = ctx->L.gu_tc;
   P1.M = 2 * sh.I / 128;
@@ -270,6 +260,7 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
     if (tm) tm->end(kStageFinalize);
     ++n;
   }
+
   TcGemmParams P2;
   P2.w = ctx->L.dn_tc;
   P2.M = sh.H / 128;
@@ -281,9 +272,9 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
   P2.gstride = 1;
   P2.gsel = 0;
   P2.row_scale = nullptr;
-  P2.post_scale = kHScale;
-  P2.mode = kTcModePartial;
-  P2.out = ws.ytc;
+  P2.post_scale = kHScale / kYScale;  // undo h's 2^-8, store y at 2^-8
+  P2.mode = kTcModeOutF16;
+  P2.out16 = ws.ytc;
   P2.out_slice = (size_t)rows * sh.H;
   P2.ldo = sh.H;
   P2.I = sh.I;
@@ -295,25 +286,6 @@ int run_experts_tc(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* ou
   if (launch_combine_tc(sh, ws, pl, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageCombine);
   ctx->launches += n;
-  return MOE_OK;
-}
-
-int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, StageTimer* tm) {
-  if (!ctx->simt) return run_experts_tc(ctx, s, x, out, T, tm, nullptr);
-  cudaError_t e;
-  if (tm) tm->begin(kStageGateUp);
-  e = launch_gateup_simt(ctx->sh, ctx->L, ctx->ws, x, T, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (tm) tm->end(kStageGateUp);
-  if (tm) tm->begin(kStageDown);
-  e = launch_down_simt(ctx->sh, ctx->L, ctx->ws, T, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (tm) tm->end(kStageDown);
-  if (tm) tm->begin(kStageCombine);
-  e = launch_combine(ctx->sh, ctx->ws, out, T, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (tm) tm->end(kStageCombine);
-  ctx->launches += 3;
   return MOE_OK;
 }
 
@@ -371,27 +343,16 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return MOE_ERR_OOM;
   }
   workspace_layout(*cfg, ctx->sm_count, &ctx->ws, (char*)ctx->ws_mem);
-  if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess) {
-    cudaFree(ctx->ws_mem);
-    delete ctx;
-    return MOE_ERR_CUDA;
-  }
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
-  if (!make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
-      !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false)) {
-    cudaFree(ctx->ws_mem);
-    delete ctx;
-    return MOE_ERR_CUDA;
-  }
-  if (tc_configure() != cudaSuccess || router_tc_configure() != cudaSuccess ||
-      simt_configure(ctx->sh) != cudaSuccess) {
+  if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess ||
+      !make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
+      !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false) || tc_configure() != cudaSuccess ||
+      router_tc_configure() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(ctx->ws_mem);
     delete ctx;
     return MOE_ERR_CUDA;
   }
-  const char* ev = getenv("MOE_GB300_EXPERTS");
-  ctx->simt = ev && strcmp(ev, "simt") == 0;
   *out = ctx;
   return MOE_OK;
 }
@@ -405,12 +366,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   for (size_t e = 0; e < E; ++e)
     if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
-  uint8_t *gu_c, *gu_s, *dn_c, *dn_s, *gu_tc, *dn_tc;
-  uint16_t* w3;
-  float *rw, *rb, *gug, *dng;
   if (!ctx->weights_mem) {
-    ctx->weights_bytes =
-        weights_layout(c, nullptr, nullptr, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc, &dn_tc, &w3);
+    ctx->weights_bytes = weights_layout(c, nullptr, nullptr);
     if (cudaMalloc(&ctx->weights_mem, ctx->weights_bytes) != cudaSuccess) {
       cudaGetLastError();
       ctx->weights_mem = nullptr;
@@ -418,8 +375,15 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
     }
   }
   ctx->loaded = false;
-  weights_layout(c, &ctx->L, (char*)ctx->weights_mem, &gu_c, &gu_s, &dn_c, &dn_s, &rw, &rb, &gug, &dng, &gu_tc,
-                 &dn_tc, &w3);
+  WeightPtrs W;
+  weights_layout(c, &W, (char*)ctx->weights_mem);
+  ctx->L.router_w = W.router_w;
+  ctx->L.router_bias = W.router_bias;
+  ctx->L.router_w3 = W.w3;
+  ctx->L.gu_global = W.gu_global;
+  ctx->L.dn_global = W.dn_global;
+  ctx->L.gu_tc = W.gu_tc;
+  ctx->L.dn_tc = W.dn_tc;
   const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
   uint8_t* staging = nullptr;
   if (cudaMalloc(&staging, gu_cb + gu_sb + dn_cb + dn_sb) != cudaSuccess) {
@@ -433,16 +397,25 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   }
   int st = MOE_OK;
   do {
-    if (cudaMemcpy(rw, lh->router_w, H * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
-    if (lh->router_bias) {
-      if (cudaMemcpy(rb, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
-    } else if (cudaMemset(rb, 0, E * sizeof(float)) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
-    if (cudaMemcpy(gug, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
-    if (launch_router_split(ctx->sh, rw, w3, s) != cudaSuccess ||
-        !make_tmap_16(&ctx->tmap_w3, w3, ((E + 127) / 128) * 128, 3 * H, 128, true)) { st = MOE_ERR_CUDA; break; }
-    if (cudaMemcpy(dng, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+    if (cudaMemcpy(W.router_w, lh->router_w, H * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        (lh->router_bias
+             ? cudaMemcpy(W.router_bias, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice)
+             : cudaMemset(W.router_bias, 0, E * sizeof(float))) != cudaSuccess ||
+        cudaMemcpy(W.gu_global, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(W.dn_global, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+      st = MOE_ERR_CUDA;
+      break;
+    }
+    if (launch_router_split(ctx->sh, W.router_w, W.w3, s) != cudaSuccess ||
+        !make_tmap_16(&ctx->tmap_w3, W.w3, ((E + 127) / 128) * 128, 3 * H, 128, true)) {
+      st = MOE_ERR_CUDA;
+      break;
+    }
     for (size_t e = 0; e < E && st == MOE_OK; ++e) {
-      if (cudaStreamSynchronize(s) != cudaSuccess) { st = MOE_ERR_CUDA; break; }
+      if (cudaStreamSynchronize(s) != cudaSuccess) {  // the staging buffer is free again
+        st = MOE_ERR_CUDA;
+        break;
+      }
       uint8_t* sc = staging;
       uint8_t* ss = staging + gu_cb;
       uint8_t* dc = ss + gu_sb;
@@ -450,12 +423,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
       if (cudaMemcpyAsync(sc, lh->gu_codes[e], gu_cb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
           cudaMemcpyAsync(ss, lh->gu_scales[e], gu_sb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
           cudaMemcpyAsync(dc, lh->dn_codes[e], dn_cb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-          cudaMemcpyAsync(ds, lh->dn_scales[e], dn_sb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
-        st = MOE_ERR_CUDA;
-        break;
-      }
-      if (launch_repack_expert(ctx->sh, (int)e, sc, ss, dc, ds, gu_c, gu_s, dn_c, dn_s, s) != cudaSuccess ||
-          launch_repack_tc(ctx->sh, (int)e, sc, ss, dc, ds, gu_tc, dn_tc, s) != cudaSuccess) {
+          cudaMemcpyAsync(ds, lh->dn_scales[e], dn_sb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+          launch_repack_tc(ctx->sh, (int)e, sc, ss, dc, ds, W.gu_tc, W.dn_tc, s) != cudaSuccess) {
         st = MOE_ERR_CUDA;
         break;
       }
@@ -474,10 +443,10 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
   StageTimer tm(ctx, s);
-  const int nmax = ctx->simt ? 0 : tc_plan(ctx->sh, T, ctx->sm_count).nmax;
-  st = run_route(ctx, s, (const uint16_t*)x, T, &tm, nmax);
+  const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
+  st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax);
   if (st != MOE_OK) return st;
-  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, &tm);
+  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm);
 }
 
 int moe_forward_host(moe_ctx* ctx, void* stream, const void* x_host, void* out_host, int32_t T) {
@@ -521,11 +490,14 @@ int moe_get_error(moe_ctx* ctx, uint32_t* bits) {
 static int copy_route_outputs(moe_ctx* ctx, cudaStream_t s, int T, float* logits, int32_t* idx, float* w,
                               int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
   const size_t E = ctx->cfg.n_experts, k = ctx->cfg.top_k;
-  struct Item { void* dst; const void* src; size_t bytes; } items[] = {
-      {logits, ctx->ws.logits, (size_t)T * E * 4}, {idx, ctx->ws.idx, (size_t)T * k * 4},
-      {w, ctx->ws.w, (size_t)T * k * 4},           {offsets, ctx->ws.offsets, (E + 1) * 4},
-      {perm, ctx->ws.perm, (size_t)T * k * 4},     {slot, ctx->ws.slot, (size_t)T * k * 4},
-      {inv, ctx->ws.inv, (size_t)T * k * 4}};
+  struct Item {
+    void* dst;
+    const void* src;
+    size_t bytes;
+  } items[] = {{logits, ctx->ws.logits, (size_t)T * E * 4}, {idx, ctx->ws.idx, (size_t)T * k * 4},
+               {w, ctx->ws.w, (size_t)T * k * 4},           {offsets, ctx->ws.offsets, (E + 1) * 4},
+               {perm, ctx->ws.perm, (size_t)T * k * 4},     {slot, ctx->ws.slot, (size_t)T * k * 4},
+               {inv, ctx->ws.inv, (size_t)T * k * 4}};
   for (const Item& it : items)
     if (it.dst && cudaMemcpyAsync(it.dst, it.src, it.bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -538,7 +510,7 @@ int moe_debug_route(moe_ctx* ctx, void* stream, const void* x, int32_t T, float*
   if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
-  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr);
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, 0);
   if (st != MOE_OK) return st;
   return copy_route_outputs(ctx, s, T, logits, idx, w, offsets, perm, slot, inv);
 }
@@ -550,6 +522,7 @@ int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, int32_t T,
   cudaStream_t s = (cudaStream_t)stream;
   if (launch_select(ctx->sh, logits, ctx->ws.idx, ctx->ws.w, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_permute(ctx->sh, ctx->ws, ctx->ws.idx, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  ctx->launches += 4;
   return copy_route_outputs(ctx, s, T, nullptr, idx, w, offsets, perm, slot, inv);
 }
 
@@ -558,23 +531,12 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
-  const int nmax = ctx->simt ? 0 : tc_plan(ctx->sh, T, ctx->sm_count).nmax;
-  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, nmax);
+  const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, pl.nmax);
   if (st != MOE_OK) return st;
-  if (!ctx->simt) {
-    TcPlan pl;
-    st = run_experts_tc(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, nullptr, &pl);
-    if (st != MOE_OK) return st;
-    return launch_debug_hy(ctx->sh, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  }
-  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, nullptr);
+  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, pl, nullptr);
   if (st != MOE_OK) return st;
-  const size_t rows = (size_t)T * ctx->cfg.top_k;
-  if (h && cudaMemcpyAsync(h, ctx->ws.h, rows * ctx->cfg.inter * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (y && cudaMemcpyAsync(y, ctx->ws.y, rows * ctx->cfg.hidden * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return launch_debug_hy(ctx->sh, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_profile_stages(void) { return kNumStages; }
@@ -604,7 +566,8 @@ int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n) {
   for (int c = 0; c < ctx->prof_calls; ++c)
     for (int i = 0; i < n; ++i) {
       if (!ctx->prof_rec[(size_t)c * kNumStages + i]) continue;
-      cudaEvent_t a = ctx->prof_ev[((size_t)c * kNumStages + i) * 2], b = ctx->prof_ev[((size_t)c * kNumStages + i) * 2 + 1];
+      cudaEvent_t a = ctx->prof_ev[((size_t)c * kNumStages + i) * 2];
+      cudaEvent_t b = ctx->prof_ev[((size_t)c * kNumStages + i) * 2 + 1];
       if (cudaEventSynchronize(b) != cudaSuccess) return MOE_ERR_CUDA;
       float t = 0.f;
       if (cudaEventElapsedTime(&t, a, b) != cudaSuccess) return MOE_ERR_CUDA;

@@ -338,7 +338,11 @@ __global__ void __launch_bounds__(kThreadsD, 2)
           }
         } else if (n < ch.n) {
           const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
-          P.out[(size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
+          const size_t o = (size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r;
+          if (P.mode == kTcModeOutF16)
+            P.out16[o] = __half_as_ushort(__float2half_rn(fminf(fmaxf(acc * gsc * rsc, -65504.f), 65504.f)));
+          else
+            P.out[o] = acc * gsc * rsc;
         }
       }
     }
@@ -560,7 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else if (n < ch.n) {
             const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
-            P.out[(size_t)p * P.ldo + (size_t)m * 128 + r] = acc * gsc * rsc;
+            const size_t o = (size_t)p * P.ldo + (size_t)m * 128 + r;
+            if (P.mode == kTcModeOutF16)
+              P.out16[o] = __half_as_ushort(__float2half_rn(fminf(fmaxf(acc * gsc * rsc, -65504.f), 65504.f)));
+            else
+              P.out[o] = acc * gsc * rsc;
           }
         }
       }
@@ -643,8 +651,9 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
   h16[i] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
 }
 
-// out[t][c] = bf16_rne( sum over j ascending of w[t][j] * sum over s of Y[s][inv[t*k+j]][c] ).
-__global__ void combine_tc_kernel(const float* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
+// out[t][c] = bf16_rne( sum over j ascending of w[t][j] * sum over s of Y[s][inv[t*k+j]][c] ),
+// fp32 sums; Y is stored in f16 scaled by 2^-8. Thread per 4 columns.
+__global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
                                   const int32_t* __restrict__ inv, uint16_t* __restrict__ out, int H, int k) {
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -653,14 +662,16 @@ __global__ void combine_tc_kernel(const float* __restrict__ y, size_t slice, int
   for (int j = 0; j < k; ++j) {
     const int p = inv[(size_t)t * k + j];
     if (p < 0) continue;
-    const float wj = w[(size_t)t * k + j];
-    float4 v = reinterpret_cast<const float4*>(y + (size_t)p * H)[c4];
-    for (int s = 1; s < S; ++s) {
-      const float4 u = reinterpret_cast<const float4*>(y + (size_t)s * slice + (size_t)p * H)[c4];
-      v.x += u.x;
-      v.y += u.y;
-      v.z += u.z;
-      v.w += u.w;
+    const float wj = w[(size_t)t * k + j] * kYScale;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+      const uint2 u = reinterpret_cast<const uint2*>(y + (size_t)s * slice + (size_t)p * H)[c4];
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      v.x += a.x;
+      v.y += a.y;
+      v.z += b.x;
+      v.w += b.y;
     }
     acc.x = fmaf(wj, v.x, acc.x);
     acc.y = fmaf(wj, v.y, acc.y);
@@ -675,15 +686,15 @@ __global__ void combine_tc_kernel(const float* __restrict__ y, size_t slice, int
   reinterpret_cast<uint2*>(out + (size_t)t * H)[c4] = packed;
 }
 
-// Inspection: h as fp32 (undoing the 2^-8 storage scale) and y summed over K splits.
-__global__ void debug_hy_kernel(const uint16_t* __restrict__ h16, const float* __restrict__ ytc, size_t slice, int S,
-                                int rows, int I, int H, float* __restrict__ h, float* __restrict__ y) {
+// Inspection: h and y as fp32 (undoing the 2^-8 storage scales), y summed over K splits.
+__global__ void debug_hy_kernel(const uint16_t* __restrict__ h16, const uint16_t* __restrict__ ytc, size_t slice,
+                                int S, int rows, int I, int H, float* __restrict__ h, float* __restrict__ y) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (h && i < (size_t)rows * I) h[i] = __half2float(__ushort_as_half(h16[i])) * kHScale;
   if (y && i < (size_t)rows * H) {
     float v = 0.f;
-    for (int s = 0; s < S; ++s) v += ytc[(size_t)s * slice + i];
-    y[i] = v;
+    for (int s = 0; s < S; ++s) v += __half2float(__ushort_as_half(ytc[(size_t)s * slice + i]));
+    y[i] = v * kYScale;
   }
 }
 

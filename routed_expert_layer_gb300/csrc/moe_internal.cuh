@@ -29,30 +29,20 @@ enum Stage {
   kNumStages
 };
 
-// Tokens per pass of the SIMT expert kernels and the SIMT tile shapes.
-constexpr int kSimtNT = 4;        // token rows held in shared memory per pass
-constexpr int kSimtWarps = 8;     // warps per CTA, splitting K
+// Tile of the SIMT router (used by the allocation-free routing entry point).
 constexpr int kRouterTT = 16;     // router tile: tokens
 constexpr int kRouterTE = 128;    // router tile: experts (one per thread)
 
-// Repacked weight layout for the streaming kernels ("row tiles of 32"):
-//   gate/up: tile rt covers gate features 16rt..16rt+15 (tile rows 0..15) and the
-//   up features with the same indices (tile rows 16..31); for every 32-element K
-//   chunk the 32 rows' 16-byte code chunks are contiguous (512 B), and for every
-//   64-element K chunk the 32 rows' 4 scale bytes are contiguous (128 B).
-//   down: tile rt covers output rows 32rt..32rt+31, same chunking along K = I.
+// Device copy of one layer. Expert weights are repacked into the tensor-core tile
+// layout (see expert_tc.cu): [E][M tiles][K chunks of 128][9216 B].
 struct DeviceLayer {
-  const uint16_t* router_w3 = nullptr; // [E_pad][3H] bf16: three-term split of W_r, transposed
-  const uint8_t* gu_tc = nullptr;     // [E][2I/128][H/64][4608] tensor-core tile layout
-  const uint8_t* dn_tc = nullptr;     // [E][H/128][I/64][4608]
-  const float* router_w = nullptr;    // [H][E]
-  const float* router_bias = nullptr; // [E] (zeros when the caller gave none)
-  const uint8_t* gu_codes = nullptr;  // [E][I/16][H/32][32][16]
-  const uint8_t* gu_scales = nullptr; // [E][I/16][H/64][32][4]
-  const float* gu_global = nullptr;   // [E][2]
-  const uint8_t* dn_codes = nullptr;  // [E][H/32][I/32][32][16]
-  const uint8_t* dn_scales = nullptr; // [E][H/32][I/64][32][4]
-  const float* dn_global = nullptr;   // [E]
+  const float* router_w = nullptr;      // [H][E] fp32
+  const float* router_bias = nullptr;   // [E] (zeros when the caller gave none)
+  const uint16_t* router_w3 = nullptr;  // [E_pad][3H] bf16: three-term split of W_r, transposed
+  const uint8_t* gu_tc = nullptr;       // [E][2I/128][H/128][9216] gate/up tiles (rows interleaved)
+  const uint8_t* dn_tc = nullptr;       // [E][H/128][I/128][9216] down tiles
+  const float* gu_global = nullptr;     // [E][2] (gate, up) tensor scales
+  const float* dn_global = nullptr;     // [E]
 };
 
 // ---- tensor-core path ------------------------------------------------------------------
@@ -66,6 +56,10 @@ constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
 constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums
 constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes f16 h
+constexpr int kTcModeOutF16 = 2;      // epilogue writes scaled f16 values to out16
+// The down projection's output y is also kept in f16, scaled by 2^-8 (same range
+// and precision argument as h); the combine undoes the scale.
+constexpr float kYScale = 256.0f;
 
 // A run of at most nmax routed rows of one expert; every (chunk, M tile, K split)
 // is one work item of the grouped GEMM, decoded arithmetically from its index.
@@ -95,6 +89,7 @@ struct TcGemmParams {
   float post_scale = 1.f;
   int mode = kTcModePartial;
   float* out = nullptr;              // partial output [S][rows][ldo]
+  uint16_t* out16 = nullptr;         // f16 output [S][rows][ldo] (kTcModeOutF16)
   size_t out_slice = 0;
   int ldo = 0;
   uint16_t* h16 = nullptr;           // SwiGLU output [rows][I]
@@ -132,8 +127,6 @@ struct Workspace {
   int32_t* perm = nullptr;        // [T*k]
   int32_t* slot = nullptr;        // [T*k]
   int32_t* inv = nullptr;         // [T*k]
-  float* h = nullptr;             // [T*k][I]
-  float* y = nullptr;             // [T*k][H]
   uint16_t* x_stage = nullptr;    // [T][H] for moe_forward_host
   uint16_t* out_stage = nullptr;  // [T][H]
   uint32_t* err = nullptr;        // device error word
@@ -142,7 +135,7 @@ struct Workspace {
   float* row_scale = nullptr;     // [T*k] 2^-sigma of each row of xg
   uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations (x 2^-8)
   float* part1 = nullptr;         // [S1][T*k][2I] gate/up partial sums (split K only)
-  float* ytc = nullptr;           // [S2][T*k][H] down-projection partial sums
+  uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums (x 2^-8)
   TcChunk* chunks = nullptr;     // row chunks of the touched experts (count in meta[2])
   int chunk_cap = 0;
 };
@@ -169,15 +162,10 @@ cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, fl
 // nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
                            int nmax = 0);
-cudaError_t launch_gateup_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
-                               cudaStream_t s);
-cudaError_t launch_down_simt(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
-cudaError_t launch_combine(const Shape& sh, const Workspace& ws, uint16_t* out, int T, cudaStream_t s);
 
 // Large-shared-memory opt-in for the kernels that need it (call once per context).
 cudaError_t tc_configure();
 cudaError_t router_tc_configure();
-cudaError_t simt_configure(const Shape& sh);
 
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
@@ -191,10 +179,5 @@ cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& 
 cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
                              const uint8_t* dn_codes_raw, const uint8_t* dn_scales_raw, uint8_t* gu_tc, uint8_t* dn_tc,
                              cudaStream_t s);
-
-// Load-time repack of one expert from raw (caller layout) device staging buffers.
-cudaError_t launch_repack_expert(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
-                                 const uint8_t* dn_codes_raw, const uint8_t* dn_scales_raw, uint8_t* gu_codes,
-                                 uint8_t* gu_scales, uint8_t* dn_codes, uint8_t* dn_scales, cudaStream_t s);
 
 }  // namespace moe

@@ -36,6 +36,10 @@ struct moe_ctx {
   int64_t launches = 0;   // kernels enqueued so far
   CUtensorMap tmap_x{};   // f16 activation rows (B of the gate/up GEMM)
   CUtensorMap tmap_h{};   // f16 SwiGLU rows (B of the down GEMM)
+  CUtensorMap tmap_x64{}; // the same two tensors in boxes of 64 and 128 rows
+  CUtensorMap tmap_h64{};
+  CUtensorMap tmap_x128{};
+  CUtensorMap tmap_h128{};
   CUtensorMap tmap_w3{};  // bf16 three-term router weights (A of the router GEMM)
   // profiling
   int prof_max = 0;
@@ -251,7 +255,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P1.I = sh.I;
   P1.err = ws.err;
   if (tm) tm->begin(kStageGateUp);
-  if (launch_gemm(pl, ctx->tmap_x, P1, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(pl, ctx->tmap_x, ctx->tmap_x64, ctx->tmap_x128, P1, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageGateUp);
   int n = 4;
   if (pl.S1 > 1) {
@@ -280,7 +284,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P2.I = sh.I;
   P2.err = ws.err;
   if (tm) tm->begin(kStageDown);
-  if (launch_gemm(pl, ctx->tmap_h, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(pl, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageDown);
   if (tm) tm->begin(kStageCombine);
   if (launch_combine_tc(sh, ws, pl, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -346,7 +350,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
   if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess ||
       !make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
-      !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false) || tc_configure() != cudaSuccess ||
+      !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false) ||
+      !make_tmap_16(&ctx->tmap_x64, ctx->ws.xg, rows, cfg->hidden, 64, false) ||
+      !make_tmap_16(&ctx->tmap_h64, ctx->ws.h16, rows, cfg->inter, 64, false) ||
+      !make_tmap_16(&ctx->tmap_x128, ctx->ws.xg, rows, cfg->hidden, 128, false) ||
+      !make_tmap_16(&ctx->tmap_h128, ctx->ws.h16, rows, cfg->inter, 128, false) || tc_configure() != cudaSuccess ||
       router_tc_configure() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(ctx->ws_mem);

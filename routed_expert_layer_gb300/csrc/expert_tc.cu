@@ -40,13 +40,12 @@ using namespace ptx;
 namespace {
 
 constexpr int kChunkK = 128;         // K elements per pipeline stage (8 MMAs of K=16)
-constexpr int kCodeBytes = 8192;     // one stage of A codes: [4 units of 16 B][128 rows][16 B]
-constexpr int kRawBytes = 9216;      // + scales [128 rows][8 B]
+constexpr int kSlice = 4608;         // one tile's 64-element K half: [2 units][128 rows][16 B] codes + [128][4 B] scales
+constexpr int kRawBytes = 2 * kSlice;  // one tile's 128-element K chunk
 constexpr int kRawSlot = 10240;      // raw slot rounded up to the 1024 B swizzle atom
 constexpr int kBoxRows = 16;         // activation rows per TMA box (64 f16 = 128 B per row)
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;
 constexpr int kAStages = 3;          // A tiles in TMEM, 64 columns each
 constexpr int kACols = 64;
 
@@ -180,7 +179,9 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
         const TcChunk ch = P.chunks[ci];
         const int nb = (ch.n + kBoxRows - 1) / kBoxRows;
-        const uint8_t* wsrc = P.w + ((size_t)(ch.e * P.M + m) * P.KC + (size_t)s * kc_per) * kRawBytes;
+        // slice (m, kc, h) of expert e sits at (((e*M/2 + m/2)*KC + kc)*2 + h)*2 + m%2 slices
+        const uint8_t* wsrc = P.w + ((size_t)(ch.e * (P.M / 2) + (m >> 1)) * P.KC + (size_t)s * kc_per) * 4 * kSlice +
+                              (size_t)(m & 1) * kSlice;
         const uint32_t tx = kRawBytes + nb * 2 * kBoxBytes;
         for (int c = 0; c < kc_per; ++c) {
           if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
@@ -189,7 +190,8 @@ __global__ void __launch_bounds__(kThreadsD, 2)
           }
           uint8_t* sb = smem + (size_t)rs.idx * kStage;
           mbar_arrive_expect_tx(&full[rs.idx], tx);
-          bulk_g2s(sb, wsrc + (size_t)c * kRawBytes, kRawBytes, &full[rs.idx]);
+          bulk_g2s(sb, wsrc + (size_t)c * 4 * kSlice, kSlice, &full[rs.idx]);
+          bulk_g2s(sb + kSlice, wsrc + (size_t)c * 4 * kSlice + 2 * kSlice, kSlice, &full[rs.idx]);
           const int kx = (s * kc_per + c) * kChunkK;
           for (int b = 0; b < nb; ++b) {
             tma_2d(sb + kRawSlot + b * kBoxBytes, &tmap_b, kx, ch.p0 + b * kBoxRows, &full[rs.idx]);
@@ -261,9 +263,9 @@ __global__ void __launch_bounds__(kThreadsD, 2)
     const int half = dw >> 2;      // which 64-element half of a 128-element stage
     const int r = 32 * q + lane;   // tile row owned by this thread
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int code_off0 = ((2 * half) * 128 + r) * 16;
-    const int code_off1 = ((2 * half + 1) * 128 + r) * 16;
-    const int scale_off = kCodeBytes + half * 512 + r * 4;
+    const int code_off0 = half * kSlice + r * 16;
+    const int code_off1 = half * kSlice + (128 + r) * 16;
+    const int scale_off = half * kSlice + 4096 + r * 4;
     Ring rs, ra;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
@@ -361,13 +363,19 @@ __global__ void __launch_bounds__(kThreadsD, 2)
 // Each CTA computes two adjacent 128-row weight tiles (M tiles 2mp and 2mp+1) of one
 // row chunk, so every activation tile staged in shared memory feeds twice the MMA
 // work; stages are 64 elements of K (one 128-byte swizzle row), six deep. TMEM: two
-// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns.
+// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Sixteen
+// dequantisation warps (four per SM sub-partition) each convert 32 weights of one
+// row per stage and later run the epilogue for half of the accumulator columns.
+constexpr int kDequantWarpsP = 16;
+constexpr int kThreadsP = (2 + kDequantWarpsP) * 32;
+
 template <int NMAX, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_mt2_kernel(const __grid_constant__ CUtensorMap tmap_b, const TcGemmParams P) {
+__global__ void __launch_bounds__(kThreadsP, 1)
+    grouped_gemm_mt2_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_b64,
+                            const __grid_constant__ CUtensorMap tmap_b128, const TcGemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  constexpr int kHalfRaw = 4608;              // one tile's 64-element K slice: 4096 B codes + 512 B scales
+  constexpr int kHalfRaw = kSlice;            // one tile's 64-element K slice: 4096 B codes + 512 B scales
   constexpr int kASlot = 10240;               // two tiles' raw slices, padded to 1024
   constexpr int kStage = kASlot + NMAX * 128;
   constexpr int kA2 = 2;                      // A stages in TMEM (each 2 tiles x 32 columns)
@@ -386,14 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDequantWarps + 1);
+      mbar_init(&empty[s], kDequantWarpsP + 1);
     }
     for (int a = 0; a < kA2; ++a) {
-      mbar_init(&afull[a], kDequantWarps);
+      mbar_init(&afull[a], kDequantWarpsP);
       mbar_init(&aempty[a], 1);
     }
     mbar_init(accfull, 1);
-    mbar_init(accempty, kDequantWarps);
+    mbar_init(accempty, kDequantWarpsP);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -418,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const int ci = it / MP, mp = it - ci * MP;
         const TcChunk ch = P.chunks[ci];
-        const int nb = (ch.n + kBoxRows - 1) / kBoxRows;
-        const uint8_t* w0 = P.w + (size_t)(ch.e * P.M + 2 * mp) * P.KC * kRawBytes;
-        const uint8_t* w1 = w0 + (size_t)P.KC * kRawBytes;
+        const int nb = (ch.n + kBoxRows - 1) / kBoxRows;  // 16-row units of the activation tile
+        // the two tiles' slices of K half h are adjacent: one copy per stage
+        const uint8_t* wsrc = P.w + (size_t)(ch.e * (P.M / 2) + mp) * P.KC * 4 * kSlice;
         const uint32_t tx = 2 * kHalfRaw + nb * kBoxBytes;
         for (int c = 0; c < n64; ++c) {
           if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
@@ -428,14 +436,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sb = smem + (size_t)rs.idx * kStage;
-          const size_t off = (size_t)(c >> 1) * kRawBytes;
-          const int h = c & 1;
           mbar_arrive_expect_tx(&full[rs.idx], tx);
-          bulk_g2s(sb, w0 + off + h * 4096, 4096, &full[rs.idx]);
-          bulk_g2s(sb + 4096, w0 + off + kCodeBytes + h * 512, 512, &full[rs.idx]);
-          bulk_g2s(sb + kHalfRaw, w1 + off + h * 4096, 4096, &full[rs.idx]);
-          bulk_g2s(sb + kHalfRaw + 4096, w1 + off + kCodeBytes + h * 512, 512, &full[rs.idx]);
-          for (int b = 0; b < nb; ++b)
+          bulk_g2s(sb, wsrc + (size_t)c * 2 * kSlice, 2 * kSlice, &full[rs.idx]);
+          // activation rows in as few boxes as possible: 128, 64, then 16 rows
+          int b = 0;
+          for (; b + 8 <= nb; b += 8)
+            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b128, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
+          for (; b + 4 <= nb; b += 4)
+            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b64, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
+          for (; b < nb; ++b)
             tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
           ++issued;
           rs.next(NS);
@@ -494,13 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int dw = warp - 2;
-    const int q = warp & 3;
-    const int t = dw >> 2;  // which of the two weight tiles this warp serves
+    const int q = warp & 3;          // TMEM lane quarter of this warp
+    const int t = (dw >> 2) & 1;     // which of the two weight tiles this warp serves
+    const int hh = dw >> 3;          // which 32-element half of the 64-element stage
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int code_off0 = t * kHalfRaw + r * 16;
-    const int code_off1 = t * kHalfRaw + (128 + r) * 16;
-    const int scale_off = t * kHalfRaw + 4096 + r * 4;
+    const int code_off = t * kHalfRaw + (hh * 128 + r) * 16;
+    const int scale_off = t * kHalfRaw + 4096 + r * 4 + hh * 2;
     Ring rs, ra;
     int local = 0;
     bool ok = true;
@@ -511,18 +520,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* raw = smem + (size_t)rs.idx * kStage;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(raw + code_off0);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(raw + code_off1);
-        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
+        const uint4 cw = *reinterpret_cast<const uint4*>(raw + code_off);
+        const uint32_t s2w = *reinterpret_cast<const uint16_t*>(raw + scale_off);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[rs.idx]);
-        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
-        const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
-        uint32_t v[32];
-        dequant_unit(c0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
-        dequant_unit(c1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
+        const uint32_t s01 = e4m3x2_to_f16x2(s2w);
+        uint32_t v[16];
+        dequant_unit(cw, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
         __syncwarp();
-        tmem_st32(tmem + lane_base + (uint32_t)(ra.idx * 64 + t * 32), v);
+        tmem_st16(tmem + lane_base + (uint32_t)(ra.idx * 64 + t * 32 + hh * 16), v);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TcChunk ch = P.chunks[ci];
       const int N = ((ch.n + 15) / 16) * 16;
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
-      for (int c0 = 0; c0 < N; c0 += 8) {
+      for (int c0 = hh * (N / 2); c0 < (hh + 1) * (N / 2); c0 += 8) {
         uint32_t v[8];
         __syncwarp();
         tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(t * NMAX + c0), v);
@@ -588,48 +594,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- activation rows in f16 ---------------------------------------------------------------
 
-// Routed row p <- token perm[p], converted to f16 after scaling by 2^sigma so the
-// row's largest magnitude lands in [2^13, 2^14): the conversion of bf16 values is
-// then exact (f16 has 11 significant bits) down to 2^-28 of the row maximum.
-// row_scale[p] = 2^-sigma undoes it in the epilogue. One warp per routed row.
-__global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                    uint16_t* __restrict__ xg, float* __restrict__ row_scale, int rows, int H) {
-  const int p = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+// Token t's row, converted to f16 after scaling by 2^sigma so the row's largest
+// magnitude lands in [2^13, 2^14) (the conversion of bf16 values is then exact down to
+// 2^-28 of the row maximum), is written to each of its k routed rows inv[t*k+j];
+// row_scale[p] = 2^-sigma undoes the scaling in the epilogue. One warp per token:
+// the row is read once into registers (H <= 14336 -> at most 56 uint4 per lane).
+template <int MAXV>
+__global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv,
+                                    uint16_t* __restrict__ xg, float* __restrict__ row_scale, int T, int H, int k) {
+  const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  if (p >= rows) return;
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm[p] * H);
+  if (t >= T) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
   const int n8 = H / 8;
+  uint4 v[MAXV];
   uint32_t mx = 0;
-  for (int i = lane; i < n8; i += 32) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = (c < n8) ? src[c] : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  // bf16 magnitude bits: exponent field in bits 7..14
   int sigma = 0;
   if (mx != 0) {
-    const int e = (int)((mx >> 7) & 0xFF) - 127;  // floor(log2(max)) for normal values
+    const int e = (int)((mx >> 7) & 0xFF) - 127;  // floor(log2(max)) from the bf16 exponent field
     sigma = 13 - e;
     sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
   }
   const float sc = __int_as_float((sigma + 127) << 23);  // exactly 2^sigma
-  if (lane == 0) row_scale[p] = __int_as_float((127 - sigma) << 23);
-  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
-  for (int i = lane; i < n8; i += 32) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(w[j] << 16) * sc;
-      const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
-      const __half2 hh = __floats2half2_rn(lo, hi);
+      const __half2 hh = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
       o[j] = *reinterpret_cast<const uint32_t*>(&hh);
     }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    v[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int p = inv[(size_t)t * k + j];
+    if (p < 0) continue;
+    if (lane == 0) row_scale[p] = __int_as_float((127 - sigma) << 23);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int c = lane + 32 * i;
+      if (c < n8) dst[c] = v[i];
+    }
   }
 }
 
@@ -652,38 +669,58 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
 }
 
 // out[t][c] = bf16_rne( sum over j ascending of w[t][j] * sum over s of Y[s][inv[t*k+j]][c] ),
-// fp32 sums; Y is stored in f16 scaled by 2^-8. Thread per 4 columns.
+// fp32 sums; Y is stored in f16 scaled by 2^-8. Thread per 8 columns; the k rows'
+// loads of a split are issued together.
+__device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    a[2 * i] = fmaf(wj, f.x, a[2 * i]);
+    a[2 * i + 1] = fmaf(wj, f.y, a[2 * i + 1]);
+  }
+}
+
 __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
                                   const int32_t* __restrict__ inv, uint16_t* __restrict__ out, int H, int k) {
   const int t = blockIdx.y;
-  const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c4 * 4 >= H) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int p = inv[(size_t)t * k + j];
-    if (p < 0) continue;
-    const float wj = w[(size_t)t * k + j] * kYScale;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-      const uint2 u = reinterpret_cast<const uint2*>(y + (size_t)s * slice + (size_t)p * H)[c4];
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      v.x += a.x;
-      v.y += a.y;
-      v.z += b.x;
-      v.w += b.y;
+  const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c8 * 8 >= H) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (S == 1) {
+    uint4 u[32];
+    float wj[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < k) {
+        const int p = inv[(size_t)t * k + j];
+        wj[j] = (p < 0) ? 0.f : w[(size_t)t * k + j] * kYScale;
+        u[j] = (p < 0) ? make_uint4(0, 0, 0, 0) : reinterpret_cast<const uint4*>(y + (size_t)p * H)[c8];
+      }
     }
-    acc.x = fmaf(wj, v.x, acc.x);
-    acc.y = fmaf(wj, v.y, acc.y);
-    acc.z = fmaf(wj, v.z, acc.z);
-    acc.w = fmaf(wj, v.w, acc.w);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < k) acc_f16x8(u[j], wj[j], acc);
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int p = inv[(size_t)t * k + j];
+      if (p < 0) continue;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < S; ++s)
+        acc_f16x8(reinterpret_cast<const uint4*>(y + (size_t)s * slice + (size_t)p * H)[c8], 1.f, v);
+      const float wj = w[(size_t)t * k + j] * kYScale;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&lo);
-  packed.y = *reinterpret_cast<uint32_t*>(&hi);
-  reinterpret_cast<uint2*>(out + (size_t)t * H)[c4] = packed;
+  uint4 packed;
+  uint32_t* pk = reinterpret_cast<uint32_t*>(&packed);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    pk[i] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  reinterpret_cast<uint4*>(out + (size_t)t * H)[c8] = packed;
 }
 
 // Inspection: h and y as fp32 (undoing the 2^-8 storage scales), y summed over K splits.
@@ -709,32 +746,33 @@ cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& 
 
 // ---- load-time repack into the tensor-core tile layout ------------------------------------------
 
-// Tile layout: [M tiles][K chunks of 128][9216 B]: codes as [unit (4)][row (128)][16 B]
-// (unit u = elements 32u..32u+31 of the chunk), then scales as [half (2)][row (128)][4 B]
-// (half h = the E4M3 scales of elements 64h..64h+63), so each 64-element half of a
-// chunk is two contiguous pieces: codes [4096h, 4096h+4096) and scales [8192+512h, +512).
+// Tile layout per expert: [M/2 tile pairs][K chunks of 128][K half h (2)][tile of the pair (2)][4608 B].
+// A 4608-byte slice holds one tile's 64 elements of K for its 128 rows: codes as
+// [unit (2)][row (128)][16 B] (unit u = elements 32u..32u+31 of the half), then the
+// E4M3 scales as [row (128)][4 B]. So a 128-element chunk of one tile is two slices
+// (K halves 0 and 1) and a 64-element half of a tile pair is one 9216-byte run.
 // Gate/up tiles interleave rows: tile row 2i is gate feature 64m+i, row 2i+1 is up
 // feature 64m+i. Down tiles: row r is output feature 128m+r.
 __global__ void repack_tc_kernel(const uint8_t* __restrict__ raw_c, const uint8_t* __restrict__ raw_s,
                                  uint8_t* __restrict__ out, int K, int M, int gateup, int half_rows) {
   const int KC = K / kChunkK;
-  const size_t units = (size_t)M * KC * 640;  // 512 code units of 16 B + 128 scale units of 8 B per tile
+  const size_t units = (size_t)M * KC * 768;  // per (tile, chunk): 2 halves x (256 code units + 128 scale units)
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= units) return;
-  const size_t tile = i / 640;
-  const int u = (int)(i % 640);
+  const size_t tile = i / 768;
+  const int u = (int)(i % 768);
   const int m = (int)(tile / KC), kc = (int)(tile % KC);
-  uint8_t* dst = out + tile * kRawBytes;
-  const int r = (u < 512) ? (u % 128) : (u - 512);
+  const int h = u / 384, v = u % 384;
+  const int r = (v < 256) ? (v % 128) : (v - 256);
   const int R = gateup ? ((r & 1) ? half_rows + m * 64 + (r >> 1) : m * 64 + (r >> 1)) : m * 128 + r;
-  if (u < 512) {
-    const int unit = u / 128;
+  uint8_t* dst = out + ((((size_t)(m >> 1) * KC + kc) * 2 + h) * 2 + (m & 1)) * kSlice;
+  if (v < 256) {
+    const int unit = v / 128;
     *reinterpret_cast<uint4*>(dst + (unit * 128 + r) * 16) =
-        *reinterpret_cast<const uint4*>(raw_c + (size_t)R * (K / 2) + kc * 64 + unit * 16);
+        *reinterpret_cast<const uint4*>(raw_c + (size_t)R * (K / 2) + kc * 64 + (2 * h + unit) * 16);
   } else {
-    const uint2 sc = *reinterpret_cast<const uint2*>(raw_s + (size_t)R * (K / 16) + kc * 8);
-    *reinterpret_cast<uint32_t*>(dst + kCodeBytes + r * 4) = sc.x;        // blocks 0..3 (first 64 of K)
-    *reinterpret_cast<uint32_t*>(dst + kCodeBytes + 512 + r * 4) = sc.y;  // blocks 4..7
+    *reinterpret_cast<uint32_t*>(dst + 4096 + r * 4) =
+        *reinterpret_cast<const uint32_t*>(raw_s + (size_t)R * (K / 16) + kc * 8 + h * 4);
   }
 }
 
@@ -744,7 +782,7 @@ cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw
   const int H = sh.H, I = sh.I;
   const int M1 = 2 * I / 128, M2 = H / 128;
   const size_t per1 = (size_t)M1 * (H / kChunkK) * kRawBytes, per2 = (size_t)M2 * (I / kChunkK) * kRawBytes;
-  const size_t u1 = (size_t)M1 * (H / kChunkK) * 640, u2 = (size_t)M2 * (I / kChunkK) * 640;
+  const size_t u1 = (size_t)M1 * (H / kChunkK) * 768, u2 = (size_t)M2 * (I / kChunkK) * 768;
   repack_tc_kernel<<<(unsigned)((u1 + 255) / 256), 256, 0, s>>>(gu_codes_raw, gu_scales_raw, gu_tc + e * per1, H, M1,
                                                                 1, I);
   repack_tc_kernel<<<(unsigned)((u2 + 255) / 256), 256, 0, s>>>(dn_codes_raw, dn_scales_raw, dn_tc + e * per2, I, M2,
@@ -784,8 +822,14 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
 }
 
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s) {
-  const int rows = T * sh.k;
-  gather_x_f16_kernel<<<(rows + 7) / 8, 256, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+  const int n8 = sh.H / 8;
+  const dim3 grid((T + 7) / 8), block(256);
+  if (n8 <= 32 * 8)
+    gather_x_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+  else if (n8 <= 32 * 28)
+    gather_x_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+  else
+    gather_x_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
   return cudaGetLastError();
 }
 
@@ -814,13 +858,15 @@ cudaError_t tc_configure() {
 }
 
 template <int NMAX, int NS>
-static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
-  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreads, smem_mt2<NMAX, NS>(), s>>>(map, P);
+static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
+                                     const TcGemmParams& P, int grid, cudaStream_t s) {
+  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreadsP, smem_mt2<NMAX, NS>(), s>>>(map, map64, map128, P);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const TcGemmParams& P, cudaStream_t s) {
-  if (pl.prefill) return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages>(map, P, pl.grid, s);
+cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
+                        const TcGemmParams& P, cudaStream_t s) {
+  if (pl.prefill) return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages>(map, map64, map128, P, pl.grid, s);
   return launch_gemm_t<kTcDecodeN, kTcDecodeStages>(map, P, pl.grid, s);
 }
 
@@ -834,7 +880,7 @@ cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const T
 
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
                               cudaStream_t s) {
-  dim3 grid((sh.H / 4 + 127) / 128, T);
+  dim3 grid((sh.H / 8 + 127) / 128, T);
   combine_tc_kernel<<<grid, 128, 0, s>>>(ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.inv, out, sh.H, sh.k);
   return cudaGetLastError();
 }

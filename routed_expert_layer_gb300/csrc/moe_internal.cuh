@@ -170,7 +170,9 @@ cudaError_t router_tc_configure();
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s);
-cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const TcGemmParams& P, cudaStream_t s);
+// map: activation rows in boxes of 16 rows; map64 / map128: the same tensor in boxes of 64 / 128 rows.
+cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
+                        const TcGemmParams& P, cudaStream_t s);
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
                               cudaStream_t s);

@@ -126,7 +126,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 // Each thread of the warp stores 16 consecutive 32-bit columns of its TMEM lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16};" ::"r"(taddr),

@@ -51,7 +51,7 @@ struct DeviceLayer {
 constexpr float kHScaleInv = 1.0f / 256.0f;
 constexpr float kHScale = 256.0f;
 constexpr int kTcDecodeN = 32;        // rows per work item, decode variant
-constexpr int kTcDecodeStages = 5;    // pipeline stages, decode variant (2 CTAs per SM)
+constexpr int kTcDecodeStages = 6;    // pipeline stages, decode variant (2 CTAs per SM)
 constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
 constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums

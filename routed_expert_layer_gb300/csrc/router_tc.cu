@@ -235,7 +235,8 @@ RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count) {
   pl.small = pl.nt <= 64;
   const int base = pl.m_tiles * pl.n_tiles;
   const int grid_ctas = sm_count;  // one CTA per SM (shared memory)
-  const int want = (2 * grid_ctas + base - 1) / base;
+  // few tiles: as many K splits as fill one wave; many tiles: about two waves
+  const int want = base < grid_ctas ? grid_ctas / base : (2 * grid_ctas + base - 1) / base;
   int best = 1;
   for (int s = 1; s <= pl.kc_total / 4; ++s)
     if (pl.kc_total % s == 0 && s <= want) best = s;

@@ -42,7 +42,7 @@ namespace {
 constexpr int kChunkK = 128;         // K elements per pipeline stage (8 MMAs of K=16)
 constexpr int kSlice = 4608;         // one tile's 64-element K half: [2 units][128 rows][16 B] codes + [128][4 B] scales
 constexpr int kRawBytes = 2 * kSlice;  // one tile's 128-element K chunk
-constexpr int kRawSlot = 10240;      // raw slot rounded up to the 1024 B swizzle atom
+constexpr int kRawSlot = 9216;       // raw slot (a multiple of the 1024 B swizzle atom)
 constexpr int kBoxRows = 16;         // activation rows per TMA box (64 f16 = 128 B per row)
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kDequantWarps = 8;
@@ -175,9 +175,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       Ring rs;
       uint32_t issued = 0;
       bool ok = true;
+      TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MS] : TcChunk{0, 0, 0, 0};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
-        const TcChunk ch = P.chunks[ci];
+        const TcChunk ch = nxt;  // record of this item, loaded one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MS];
+        (void)ci;
         const int nb = (ch.n + kBoxRows - 1) / kBoxRows;
         // slice (m, kc, h) of expert e sits at (((e*M/2 + m/2)*KC + kc)*2 + h)*2 + m%2 slices
         const uint8_t* wsrc = P.w + ((size_t)(ch.e * (P.M / 2) + (m >> 1)) * P.KC + (size_t)s * kc_per) * 4 * kSlice +
@@ -220,9 +223,10 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       Ring rs, ra;
       int local = 0;
       bool ok = true;
+      TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MS] : TcChunk{0, 0, 0, 0};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
-        const int ci = it / MS;
-        const TcChunk ch = P.chunks[ci];
+        const TcChunk ch = nxt;  // loaded one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MS];
         const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
         const uint32_t idesc = idesc_f16(128, N);
         const int b = local & 1;
@@ -301,12 +305,15 @@ __global__ void __launch_bounds__(kThreadsD, 2)
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     int local = 0;
+    TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MS] : TcChunk{0, 0, 0, 0};
     for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++local) {
       const int b = local & 1;
+      const TcChunk ch = nxt;  // loaded one item ahead
+      if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MS];
       if (!mbar_wait(&accfull[b], (uint32_t)(local >> 1) & 1u, P.err)) break;
       tc_fence_after();
       const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
-      const TcChunk ch = P.chunks[ci];
+      (void)ci;
       const int N = ((ch.n + 15) / 16) * 16;
       uint32_t v[NMAX];
 #pragma unroll
@@ -423,9 +430,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       Ring rs;
       uint32_t issued = 0;
       bool ok = true;
+      TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MP] : TcChunk{0, 0, 0, 0};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const int ci = it / MP, mp = it - ci * MP;
-        const TcChunk ch = P.chunks[ci];
+        const TcChunk ch = nxt;  // loaded one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MP];
+        (void)ci;
         const int nb = (ch.n + kBoxRows - 1) / kBoxRows;  // 16-row units of the activation tile
         // the two tiles' slices of K half h are adjacent: one copy per stage
         const uint8_t* wsrc = P.w + (size_t)(ch.e * (P.M / 2) + mp) * P.KC * 4 * kSlice;
@@ -467,8 +477,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       Ring rs, ra;
       int local = 0;
       bool ok = true;
+      TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MP] : TcChunk{0, 0, 0, 0};
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
-        const TcChunk ch = P.chunks[it / MP];
+        const TcChunk ch = nxt;  // loaded one item ahead
+        if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MP];
         const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
         const uint32_t idesc = idesc_f16(128, N);
         if (local > 0) {
@@ -650,6 +662,52 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
   }
 }
 
+// The same conversion with one warp per routed row p (token perm[p]): every row is
+// produced in parallel, which is what small batches need; large batches use the
+// per-token kernel above, which reads each token row once instead of k times.
+template <int MAXV>
+__global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                       uint16_t* __restrict__ xg, float* __restrict__ row_scale, int rows, int H) {
+  const int p = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm[p] * H);
+  const int n8 = H / 8;
+  uint4 v[MAXV];
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = (c < n8) ? src[c] : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  int sigma = 0;
+  if (mx != 0) {
+    const int e = (int)((mx >> 7) & 0xFF) - 127;
+    sigma = 13 - e;
+    sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
+  }
+  const float sc = __int_as_float((sigma + 127) << 23);
+  if (lane == 0) row_scale[p] = __int_as_float((127 - sigma) << 23);
+  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int c = lane + 32 * i;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 hh = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+      o[j] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    if (c < n8) dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ---- K-split reduction + SwiGLU, and the combine --------------------------------------
 
 // h16[p][f] = f16( silu(sum_s P[s][p][2f]) * sum_s P[s][p][2f+1] * 2^-8 ) (partials already scaled).
@@ -823,13 +881,19 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
 
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s) {
   const int n8 = sh.H / 8;
-  const dim3 grid((T + 7) / 8), block(256);
-  if (n8 <= 32 * 8)
-    gather_x_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-  else if (n8 <= 32 * 28)
-    gather_x_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-  else
-    gather_x_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+  const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
+  if (T < 1024) {  // one warp per routed row
+    const int rows = T * sh.k;
+    const dim3 grid((rows + 7) / 8), block(256);
+    if (maxv == 8) gather_rows_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    else if (maxv == 28) gather_rows_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    else gather_rows_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+  } else {  // one warp per token, its k rows written from registers
+    const dim3 grid((T + 7) / 8), block(256);
+    if (maxv == 8) gather_x_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    else if (maxv == 28) gather_x_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    else gather_x_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+  }
   return cudaGetLastError();
 }
 

@@ -257,9 +257,10 @@ def profile_run(args):
     for _ in range(args.warmup + args.steps):
         moe.forward(x, out)
     torch.cuda.synchronize()
+    d, dmax = touched(moe, x, args.experts, K3["k"])
     print(json.dumps({"profile_run": True, "experts": args.experts, "T": args.T,
                       "forwards": args.warmup + args.steps, "device_error": moe.get_error(),
-                      "kernels": moe.launch_count()}), flush=True)
+                      "kernels": moe.launch_count(), "touched_experts": d, "max_rows": dmax}), flush=True)
     moe.close()
 
 
@@ -323,7 +324,9 @@ def main():
     stages = {k_: v[0] / max(1, v[1]) for k_, v in prof.items()}
     dom = max(stages, key=stages.get)
     gu_ms = stages["gateup"]
-    gu_bytes = d_avg * GU_BYTES + T * K3["H"] * 2 + T * K3["k"] * K3["I"] * 4
+    # algorithmic bytes of one gate/up launch: the touched experts' gate/up weights, x read
+    # once (bf16) and h written once (16-bit)
+    gu_bytes = d_avg * GU_BYTES + T * K3["H"] * 2 + T * K3["k"] * K3["I"] * 2
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     step_bytes = d_avg * EXPERT_BYTES + 4 * K3["H"] * K3["E"] + 2 * T * K3["H"] * 2
     traffic = None

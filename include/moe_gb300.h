@@ -150,7 +150,9 @@ MOE_API int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t
  * moe_profile_begin arms the next `max_calls` forwards; moe_profile_end waits
  * for them and writes, for each of `n` stages (n <= moe_profile_stages()), the
  * summed milliseconds and the number of launches timed. Stage names come from
- * moe_profile_stage_name(i). */
+ * moe_profile_stage_name(i). Forwards armed inside a CUDA-graph capture are timed
+ * by the graph's replays (the last replay counts); a captured forward whose graph
+ * was never replayed is not counted. */
 MOE_API int moe_profile_stages(void);
 MOE_API const char* moe_profile_stage_name(int i);
 MOE_API int moe_profile_begin(moe_ctx* ctx, int32_t max_calls);

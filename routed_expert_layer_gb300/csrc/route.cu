@@ -134,7 +134,25 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
 
 // One warp per token. Each lane holds the keys of experts lane, lane+32, ... as
 // (ordered logit << 32) | (0xFFFFFFFF - e): all keys distinct, the largest key is
-// the largest logit with the lowest index. k rounds of a warp-wide max.
+// the largest logit with the lowest index. Each of the k rounds takes the warp-wide
+// largest key with two warp reductions (largest high word, then the largest low word
+// among the lanes holding it); only the lane that owned the winner clears it and
+// recomputes its own largest key (a depth-5 tree over its 32 slots).
+__device__ __forceinline__ unsigned long long max_u64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+__device__ __forceinline__ unsigned long long lane_best(const unsigned long long (&keys)[32]) {
+  unsigned long long t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = max_u64(keys[2 * i], keys[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = max_u64(t[2 * i], t[2 * i + 1]);
+  return t[0];
+}
+
 __global__ void select_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
                               int T, int E, int k) {
   const int tok = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -148,26 +166,21 @@ __global__ void select_kernel(const float* __restrict__ logits, int32_t* __restr
     keys[i] = (e < E) ? (((unsigned long long)ordered_bits(l[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e))
                       : 0ull;
   }
-  uint32_t taken = 0;
+  unsigned long long best = lane_best(keys);
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0ull;
-    int bi = -1;
+    const uint32_t hi = (uint32_t)(best >> 32);
+    const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? (uint32_t)best : 0u);
+    const int e = (int)(0xFFFFFFFFu - mlo);
+    if (lane == j) my_e = e;
+    if ((e & 31) == lane) {  // the owner drops the winner and finds its next best
+      const unsigned long long win = ((unsigned long long)mhi << 32) | mlo;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (!((taken >> i) & 1u) && keys[i] > best) {
-        best = keys[i];
-        bi = i;
-      }
+      for (int i = 0; i < 32; ++i)
+        if (keys[i] == win) keys[i] = 0ull;
+      best = lane_best(keys);
     }
-    unsigned long long m = best;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-      m = (o > m) ? o : m;
-    }
-    if (bi >= 0 && best == m) taken |= 1u << bi;
-    if (lane == j) my_e = (int)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
   }
   const float v = (lane < k) ? l[my_e] : 0.f;
   const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);

@@ -21,10 +21,10 @@
 //   D accumulates in fp32 in tensor memory; the epilogue applies the tensor and
 //       row scales and either the SwiGLU (gate/up rows are interleaved in the tile)
 //       or writes fp32 partial sums of a K split.
-// Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread), warps 2..9
+// Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread), the other warps
 // dequantise and run the epilogue (warp w may only touch TMEM lanes 32*(w%4)..).
-// The kernel is persistent over a device-built list of work items
-// (expert, row range, M tile, K split).
+// Both variants run one persistent CTA per SM over a device-built list of work items
+// (expert, row range, M tile(s), K split).
 #include <cuda.h>
 
 #include <algorithm>
@@ -45,12 +45,10 @@ constexpr int kRawBytes = 2 * kSlice;  // one tile's 128-element K chunk
 constexpr int kRawSlot = 9216;       // raw slot (a multiple of the 1024 B swizzle atom)
 constexpr int kBoxRows = 16;         // activation rows per TMA box (64 f16 = 128 B per row)
 constexpr int kBoxBytes = kBoxRows * 128;
-constexpr int kDequantWarps = 8;
-constexpr int kAStages = 3;          // A tiles in TMEM, 64 columns each
-constexpr int kACols = 64;
+constexpr int kACols = 64;           // one A stage (128 rows x 128 K of f16) in TMEM columns
 
-__host__ __device__ constexpr uint32_t tmem_cols(int nmax) {
-  const uint32_t need = kAStages * kACols + nmax;
+__host__ __device__ constexpr uint32_t tmem_cols(int a_stages, int nmax) {
+  const uint32_t need = a_stages * kACols + nmax;
   uint32_t c = 32;
   while (c < need) c <<= 1;
   return c;
@@ -58,9 +56,9 @@ __host__ __device__ constexpr uint32_t tmem_cols(int nmax) {
 
 template <int NMAX, int NS>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 /*alignment slack*/ + (size_t)NS * (kRawSlot + 2 * NMAX * 128) + 256 /*barriers*/;
+  return 1024 /*alignment slack*/ + (size_t)NS * (kRawSlot + 2 * NMAX * 128) + 512 /*barriers*/;
 }
-static_assert(kAStages * kACols + 2 * kTcDecodeN <= 256, "two decode CTAs per SM must fit in TMEM");
+static_assert(kTcDecodeAStages * kACols + 2 * 2 * kTcDecodeN <= 256, "two decode CTAs per SM must fit in TMEM");
 
 __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* h) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
@@ -116,28 +114,38 @@ struct Ring {  // stage index and phase parity of a circular buffer of n slots
 
 }  // namespace
 
-// Grouped GEMM over the work items (chunk, M tile, K split), decode variant. Warps:
-// 0 TMA, 1 MMA, 2..9 dequantisation, 10..13 epilogue. Two accumulators in TMEM let
-// the MMA start the next item while the epilogue warps drain the previous one.
+// Grouped GEMM over the work items (chunk, M tile, K split), decode variant, two CTAs
+// per SM. A thread issues one tcgen05.mma about every 50 cycles however small N is, so
+// at decode (N <= 16) two warps issue MMAs: warp 1 takes the even K chunks of an item,
+// warp 2 the odd ones, each into its own accumulator, and the epilogue adds the two in
+// a fixed order. TMEM A stage a is free again once the MMA of the chunk that used it
+// has completed, i.e. once that chunk's shared-memory stage has been released
+// (`empty`), so each chunk needs a single commit. Warps: 0 TMA, 1-2 MMA, 3..10
+// dequantisation (one per TMEM lane quarter and 64-element K half), 11..14 epilogue.
+// Two accumulator sets let the MMAs of the next item overlap the epilogue of the last.
 constexpr int kEpiWarps = 4;
-constexpr int kThreadsD = (2 + kDequantWarps + kEpiWarps) * 32;
+constexpr int kDequantWarps = 8;
+constexpr int kMmaWarps = 2;
+constexpr int kThreadsD = (1 + kMmaWarps + kDequantWarps + kEpiWarps) * 32;
 
 template <int NMAX, int NS>
 __global__ void __launch_bounds__(kThreadsD, 2)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const TcGemmParams P) {
+  constexpr int kAStages = kTcDecodeAStages;
+  static_assert(NS > kAStages, "an A stage is recycled through an older shared-memory stage");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   constexpr int kBSub = NMAX * 128;          // one 64-column K half of the activation tile
   constexpr int kStage = kRawSlot + 2 * kBSub;
-  constexpr uint32_t kCols = tmem_cols(2 * NMAX);
+  static_assert(kStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+  constexpr uint32_t kCols = tmem_cols(kAStages, 2 * kMmaWarps * NMAX);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
   uint64_t* afull = empty + NS;
-  uint64_t* aempty = afull + kAStages;
-  uint64_t* accfull = aempty + kAStages;  // [2]
+  uint64_t* accfull = afull + kAStages;   // [2]
   uint64_t* accempty = accfull + 2;       // [2]
-  uint64_t* drain = accempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = accempty + 2;         // [kMmaWarps]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMmaWarps);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -145,15 +153,12 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDequantWarps + 1);
     }
-    for (int a = 0; a < kAStages; ++a) {
-      mbar_init(&afull[a], kDequantWarps);
-      mbar_init(&aempty[a], 1);
-    }
+    for (int a = 0; a < kAStages; ++a) mbar_init(&afull[a], kDequantWarps);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&accfull[b], 1);
+      mbar_init(&accfull[b], kMmaWarps);
       mbar_init(&accempty[b], kEpiWarps);
     }
-    mbar_init(drain, 1);
+    for (int w = 0; w < kMmaWarps; ++w) mbar_init(&drain[w], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(kThreadsD, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_entry();
   constexpr uint32_t acc_col = kAStages * kACols;
   const int MS = P.M * P.S;
   const int n_items = *P.n_chunks * MS;
@@ -217,52 +223,52 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         }
       }
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----
+  } else if (warp <= kMmaWarps) {
+    // ---- MMA issuers: warp 1 + mw takes the chunks c = mw, mw + 2, ... of every item ----
+    const int mw = warp - 1;
     if (lane == 0) {
-      Ring rs, ra;
       int local = 0;
+      uint32_t g0 = 0;  // CTA-wide index of the item's first chunk
       bool ok = true;
       TcChunk nxt = blockIdx.x < n_items ? P.chunks[blockIdx.x / MS] : TcChunk{0, 0, 0, 0};
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local, g0 += (uint32_t)kc_per) {
         const TcChunk ch = nxt;  // loaded one item ahead
         if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MS];
         const uint32_t N = (uint32_t)((ch.n + 15) / 16) * 16;
         const uint32_t idesc = idesc_f16(128, N);
         const int b = local & 1;
-        if (local >= 2) {  // the epilogue of item local-2 has drained this accumulator
+        if (local >= 2) {  // the epilogue of item local-2 has drained this accumulator set
           if (!mbar_wait(&accempty[b], (uint32_t)((local - 2) >> 1) & 1u, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        const uint32_t acc = tmem + acc_col + b * NMAX;
-        for (int c = 0; c < kc_per; ++c) {
-          if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&afull[ra.idx], ra.ph, P.err)) {
+        const uint32_t acc = tmem + acc_col + (uint32_t)((mw * 2 + b) * NMAX);
+        for (int c = mw; c < kc_per; c += kMmaWarps) {
+          const uint32_t g = g0 + (uint32_t)c;
+          const int si = (int)(g % NS), ai = (int)(g % kAStages);
+          if (!mbar_wait(&full[si], (g / NS) & 1u, P.err) || !mbar_wait(&afull[ai], (g / kAStages) & 1u, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kRawSlot);
+          const uint32_t bsm = smem_u32(smem + (size_t)si * kStage + kRawSlot);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk)
-            mma_f16_ts(acc, tmem + ra.idx * kACols + kk * 8, desc_sw128(bsm + (kk >> 2) * kBSub + (kk & 3) * 32),
-                       idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&empty[rs.idx]);
-          mma_commit(&aempty[ra.idx]);
-          rs.next(NS);
-          ra.next(kAStages);
+            mma_f16_ts(acc, tmem + ai * kACols + kk * 8, desc_sw128(bsm + (kk >> 2) * kBSub + (kk & 3) * 32),
+                       idesc, (c >= kMmaWarps || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[si]);  // frees the shared-memory stage and, through it, the A stage
         }
         if (ok) mma_commit(&accfull[b]);
       }
       // drain: every MMA this thread issued has completed before TMEM is released
-      mma_commit(drain);
-      mbar_wait(drain, 0, P.err);
+      mma_commit(&drain[mw]);
+      mbar_wait(&drain[mw], 0, P.err);
     }
-  } else if (warp < 2 + kDequantWarps) {
+  } else if (warp <= kMmaWarps + kDequantWarps) {
     // ---- dequantisation ----
-    const int dw = warp - 2;
+    const int dw = warp - 1 - kMmaWarps;
     const int q = warp & 3;        // TMEM lane quarter of this warp
     const int half = dw >> 2;      // which 64-element half of a 128-element stage
     const int r = 32 * q + lane;   // tile row owned by this thread
@@ -270,33 +276,40 @@ __global__ void __launch_bounds__(kThreadsD, 2)
     const int code_off0 = half * kSlice + r * 16;
     const int code_off1 = half * kSlice + (128 + r) * 16;
     const int scale_off = half * kSlice + 4096 + r * 4;
-    Ring rs, ra;
+    uint32_t g = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      for (int c = 0; c < kc_per; ++c) {
-        if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&aempty[ra.idx], ra.ph ^ 1u, P.err)) {
+      for (int c = 0; c < kc_per; ++c, ++g) {
+        const int si = (int)(g % NS), ai = (int)(g % kAStages);
+        if (!mbar_wait(&full[si], (g / NS) & 1u, P.err)) {
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + (size_t)rs.idx * kStage;
+        if (g >= (uint32_t)kAStages) {  // the MMA of chunk g - kAStages has released A stage ai
+          const uint32_t go = g - kAStages;
+          if (!mbar_wait(&empty[go % NS], (go / NS) & 1u, P.err)) {
+            ok = false;
+            break;
+          }
+        }
+        const uint8_t* raw = smem + (size_t)si * kStage;
         const uint4 c0 = *reinterpret_cast<const uint4*>(raw + code_off0);
         const uint4 c1 = *reinterpret_cast<const uint4*>(raw + code_off1);
         const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[rs.idx]);
+        if (lane == 0) mbar_arrive(&empty[si]);
         const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
         const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
         uint32_t v[32];
         dequant_unit(c0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
         dequant_unit(c1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
         __syncwarp();
-        tmem_st32(tmem + lane_base + (uint32_t)(ra.idx * kACols + half * 32), v);
+        tc_fence_after();
+        tmem_st32(tmem + lane_base + (uint32_t)(ai * kACols + half * 32), v);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[ra.idx]);
-        rs.next(NS);
-        ra.next(kAStages);
+        if (lane == 0) mbar_arrive(&afull[ai]);
       }
     }
   } else {
@@ -315,14 +328,17 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       const int ci = it / MS, rem = it - ci * MS, m = rem / P.S, s = rem - m * P.S;
       (void)ci;
       const int N = ((ch.n + 15) / 16) * 16;
-      uint32_t v[NMAX];
+      uint32_t v[kMmaWarps][NMAX];
 #pragma unroll
-      for (int c0 = 0; c0 < NMAX; c0 += 8) {
-        if (c0 < N) {
-          __syncwarp();
-          tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(b * NMAX + c0), *reinterpret_cast<uint32_t(*)[8]>(v + c0));
+      for (int w = 0; w < kMmaWarps; ++w)
+#pragma unroll
+        for (int c0 = 0; c0 < NMAX; c0 += 8) {
+          if (c0 < N && w < kc_per) {  // an item of one K chunk only has the first accumulator
+            __syncwarp();
+            tmem_ld8(tmem + lane_base + acc_col + (uint32_t)((w * 2 + b) * NMAX + c0),
+                     *reinterpret_cast<uint32_t(*)[8]>(&v[w][c0]));
+          }
         }
-      }
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -332,7 +348,7 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       for (int n = 0; n < NMAX; ++n) {
         if (n >= N) break;
         const int p = ch.p0 + n;
-        const float acc = __uint_as_float(v[n]);
+        const float acc = kc_per > 1 ? __uint_as_float(v[0][n]) + __uint_as_float(v[1][n]) : __uint_as_float(v[0][n]);
         if (P.mode == kTcModeSwiglu) {
           // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
           const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
@@ -420,6 +436,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_entry();
   constexpr uint32_t acc_col = kA2 * 64;
   const int MP = P.M / 2;
   const int n_items = *P.n_chunks * MP;
@@ -614,6 +631,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 template <int MAXV>
 __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv,
                                     uint16_t* __restrict__ xg, float* __restrict__ row_scale, int T, int H, int k) {
+  pdl_entry();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -668,6 +686,7 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
 template <int MAXV>
 __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                        uint16_t* __restrict__ xg, float* __restrict__ row_scale, int rows, int H) {
+  pdl_entry();
   const int p = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= rows) return;
@@ -713,6 +732,7 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
 // h16[p][f] = f16( silu(sum_s P[s][p][2f]) * sum_s P[s][p][2f+1] * 2^-8 ) (partials already scaled).
 __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t slice, int S, int rows, int I,
                                        uint16_t* __restrict__ h16) {
+  pdl_entry();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)rows * I) return;
   const size_t p = i / I, f = i % I;
@@ -741,6 +761,7 @@ __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
 
 __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
                                   const int32_t* __restrict__ inv, uint16_t* __restrict__ out, int H, int k) {
+  pdl_entry();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c8 * 8 >= H) return;
@@ -880,28 +901,28 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
 }
 
 cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s) {
+  cudaError_t e;
   const int n8 = sh.H / 8;
   const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
   if (T < 1024) {  // one warp per routed row
     const int rows = T * sh.k;
     const dim3 grid((rows + 7) / 8), block(256);
-    if (maxv == 8) gather_rows_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
-    else if (maxv == 28) gather_rows_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
-    else gather_rows_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
   } else {  // one warp per token, its k rows written from registers
     const dim3 grid((T + 7) / 8), block(256);
-    if (maxv == 8) gather_x_f16_kernel<8><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-    else if (maxv == 28) gather_x_f16_kernel<28><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-    else gather_x_f16_kernel<56><<<grid, block, 0, s>>>(x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_x_f16_kernel<28>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    else e = launch_pdl(gather_x_f16_kernel<56>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <int NMAX, int NS>
 static cudaError_t launch_gemm_t(const CUtensorMap& map, const TcGemmParams& P, int grid, cudaStream_t s) {
   const size_t smem = gemm_smem_bytes<NMAX, NS>();
-  grouped_gemm_kernel<NMAX, NS><<<grid, kThreadsD, smem, s>>>(map, P);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<NMAX, NS>, dim3(grid), dim3(kThreadsD), smem, s, map, P);
 }
 
 template <int NMAX, int NS>
@@ -924,8 +945,8 @@ cudaError_t tc_configure() {
 template <int NMAX, int NS>
 static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                                      const TcGemmParams& P, int grid, cudaStream_t s) {
-  grouped_gemm_mt2_kernel<NMAX, NS><<<grid, kThreadsP, smem_mt2<NMAX, NS>(), s>>>(map, map64, map128, P);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_mt2_kernel<NMAX, NS>, dim3(grid), dim3(kThreadsP), smem_mt2<NMAX, NS>(), s, map,
+                    map64, map128, P);
 }
 
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
@@ -937,16 +958,15 @@ cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensor
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s) {
   const int rows = T * sh.k;
   const size_t n = (size_t)rows * sh.I;
-  swiglu_finalize_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.part1, (size_t)rows * 2 * sh.I, pl.S1, rows,
-                                                                      sh.I, ws.h16);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_finalize_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ws.part1,
+                    (size_t)rows * 2 * sh.I, pl.S1, rows, sh.I, ws.h16);
 }
 
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
                               cudaStream_t s) {
   dim3 grid((sh.H / 8 + 127) / 128, T);
-  combine_tc_kernel<<<grid, 128, 0, s>>>(ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.inv, out, sh.H, sh.k);
-  return cudaGetLastError();
+  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.inv, out,
+                    sh.H, sh.k);
 }
 
 }  // namespace moe

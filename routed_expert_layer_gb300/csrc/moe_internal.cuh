@@ -7,9 +7,43 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/moe_gb300.h"
 
 namespace moe {
+
+// ---- programmatic dependent launch ----------------------------------------------------
+// Every kernel of the forward is launched with programmatic stream serialisation. It
+// waits for the kernel before it (griddepcontrol.wait: that grid has completed and its
+// writes are visible) before it touches any memory, and only then lets the kernel after
+// it launch (griddepcontrol.launch_dependents), so at most two kernels overlap: one
+// running, the next one launched and in its prologue. Launch latency and prologues
+// (barrier setup, tensor-memory allocation) are hidden; results cannot change. When a
+// kernel is launched without the attribute both instructions do nothing.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  return [&](std::remove_cv_t<KArgs>... a) {
+    void* p[] = {(void*)&a...};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, (const void*)kernel, p);
+  }(std::forward<Args>(args)...);
+}
 
 // Device error word bits (also documented in moe_get_error).
 constexpr uint32_t kErrExpertRange = 1u;
@@ -50,8 +84,9 @@ struct DeviceLayer {
 // the absolute error stays under 2^-17); the down projection's epilogue undoes it.
 constexpr float kHScaleInv = 1.0f / 256.0f;
 constexpr float kHScale = 256.0f;
-constexpr int kTcDecodeN = 32;        // rows per work item, decode variant
-constexpr int kTcDecodeStages = 6;    // pipeline stages, decode variant (2 CTAs per SM)
+constexpr int kTcDecodeN = 16;        // rows per work item, decode variant
+constexpr int kTcDecodeStages = 8;    // shared-memory pipeline stages, decode variant (two CTAs per SM)
+constexpr int kTcDecodeAStages = 3;   // dequantised A stages in TMEM, decode variant
 constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
 constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums

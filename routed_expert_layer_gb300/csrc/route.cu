@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kRouterTE) router_partial_kernel(const uint16_
                                                                     const float* __restrict__ W,
                                                                     float* __restrict__ part, int T, int H, int E,
                                                                     int KS) {
+  pdl_entry();
   __shared__ float xs[64][kRouterTT];
   const int t0 = blockIdx.x * kRouterTT;
   const int e = blockIdx.y * kRouterTE + threadIdx.x;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kRouterTE) router_partial_kernel(const uint16_
 // logits[t][e] = sum over splits s ascending of part[s][t][e], plus bias[e].
 __global__ void router_reduce_kernel(const float* __restrict__ part, const float* __restrict__ bias,
                                      float* __restrict__ logits, int T, int E, int S) {
+  pdl_entry();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t n = (size_t)T * E;
   if (i >= n) return;
@@ -105,9 +107,8 @@ __global__ void router_reduce_kernel(const float* __restrict__ part, const float
 cudaError_t launch_router_reduce(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S,
                                  cudaStream_t s) {
   const size_t n = (size_t)T * sh.E;
-  router_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.router_part, L.router_bias, ws.logits, T, sh.E,
-                                                                    S);
-  return cudaGetLastError();
+  return launch_pdl(router_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ws.router_part,
+                    L.router_bias, ws.logits, T, sh.E, S);
 }
 
 cudaError_t launch_router(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
@@ -155,6 +156,7 @@ __device__ __forceinline__ unsigned long long lane_best(const unsigned long long
 
 __global__ void select_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
                               int T, int E, int k) {
+  pdl_entry();
   const int tok = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= T) return;
@@ -197,8 +199,7 @@ __global__ void select_kernel(const float* __restrict__ logits, int32_t* __restr
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s) {
   const int warps_per_block = 8;
   const int blocks = (T + warps_per_block - 1) / warps_per_block;
-  select_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(logits, idx, w, T, sh.E, sh.k);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, s, logits, idx, w, T, sh.E, sh.k);
 }
 
 // ---- S3 histogram / prefix sum / permutation --------------------------------------------------
@@ -207,6 +208,7 @@ cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, fl
 // 256 threads = 8 chunks; atomicOr makes the masks independent of thread order.
 __global__ void __launch_bounds__(256) perm_masks_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ masks,
                                                          uint32_t* __restrict__ err, int T, int E, int k) {
+  pdl_entry();
   extern __shared__ uint32_t msk[];  // [8][E]
   for (int i = threadIdx.x; i < 8 * E; i += 256) msk[i] = 0u;
   __syncthreads();
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restr
                                                          int32_t* __restrict__ meta, int T, int E,
                                                          TcChunk* __restrict__ chunks, int nmax, int chunk_cap,
                                                          uint32_t* __restrict__ err) {
+  pdl_entry();
   __shared__ int totals[3];
   __shared__ int max_rows;
   const int e = threadIdx.x;
@@ -312,6 +315,7 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint3
                                     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
                                     int32_t* __restrict__ perm, int32_t* __restrict__ slot, int32_t* __restrict__ inv,
                                     int T, int E, int k) {
+  pdl_entry();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * k) return;
   const int t = i / k, j = i % k;
@@ -331,13 +335,16 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint3
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
                            int nmax) {
   const int blocks = (T + 255) / 256;
-  perm_masks_kernel<<<blocks, 256, 8 * sh.E * sizeof(uint32_t), s>>>(idx, ws.masks, ws.err, T, sh.E, sh.k);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(ws.masks, ws.chunk_base, ws.counts, ws.offsets, ws.active, ws.meta, T, sh.E,
-                                      nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err);
+  cudaError_t e = launch_pdl(perm_masks_kernel, dim3(blocks), dim3(256), 8 * sh.E * sizeof(uint32_t), s, idx,
+                             ws.masks, ws.err, T, sh.E, sh.k);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, ws.masks, ws.chunk_base, ws.counts, ws.offsets,
+                 ws.active, ws.meta, T, sh.E, nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap,
+                 ws.err);
+  if (e != cudaSuccess) return e;
   const int n = T * sh.k;
-  perm_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(idx, ws.masks, ws.chunk_base, ws.offsets, ws.perm, ws.slot,
-                                                      ws.inv, T, sh.E, sh.k);
-  return cudaGetLastError();
+  return launch_pdl(perm_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, s, idx, ws.masks, ws.chunk_base,
+                    ws.offsets, ws.perm, ws.slot, ws.inv, T, sh.E, sh.k);
 }
 
 }  // namespace moe

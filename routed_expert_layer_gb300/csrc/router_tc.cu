@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_entry();
   const int KS = P.S;  // K splits
   const int n_items = P.m_tiles * P.n_tiles * KS;
   const int kc_per = P.kc_total / KS;
@@ -263,8 +264,7 @@ cudaError_t router_tc_configure() {
 template <int NMAX>
 static cudaError_t launch_router_tc_t(const CUtensorMap& mw, const CUtensorMap& mx, const RouterTcParams& P, int grid,
                                       cudaStream_t s) {
-  router_tc_kernel<NMAX><<<grid, kRThreads, router_smem_bytes<NMAX>(), s>>>(mw, mx, P);
-  return cudaGetLastError();
+  return launch_pdl(router_tc_kernel<NMAX>, dim3(grid), dim3(kRThreads), router_smem_bytes<NMAX>(), s, mw, mx, P);
 }
 
 cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx,

@@ -21,6 +21,8 @@
 
 using namespace moe;
 
+thread_local bool moe::g_launch_pdl = false;
+
 struct moe_ctx {
   moe_config cfg{};
   Shape sh{};
@@ -59,6 +61,12 @@ struct DeviceGuard {
   ~DeviceGuard() {
     if (prev >= 0) cudaSetDevice(prev);
   }
+};
+
+// Programmatic dependent launch for the kernels one forward enqueues (decode sizes).
+struct PdlScope {
+  explicit PdlScope(bool on) { g_launch_pdl = on; }
+  ~PdlScope() { g_launch_pdl = false; }
 };
 
 const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep", "gateup", "finalize", "down", "combine"};
@@ -452,6 +460,7 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   cudaStream_t s = (cudaStream_t)stream;
   StageTimer tm(ctx, s);
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
+  PdlScope pdl(!pl.prefill);
   st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax);
   if (st != MOE_OK) return st;
   return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm);

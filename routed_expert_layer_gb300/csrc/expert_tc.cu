@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             const float rsc = P.row_scale[p];
             const float gv = acc * gsc * rsc;
             const float uv = other * o_gsc * rsc;
-            const float hv = gv / (1.f + expf(-gv)) * uv * kHScaleInv;
+            const float hv = gv / (1.f + __expf(-gv)) * uv * kHScaleInv;
             const int f = m * 64 + (r >> 1);
             P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
           }
@@ -578,6 +578,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
       for (int c0 = hh * (N / 2); c0 < (hh + 1) * (N / 2); c0 += 8) {
         uint32_t v[8];
+        float rs8[8];  // row scales of the 8 rows, loaded ahead of the accumulator read
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          rs8[i] = (P.mode == kTcModeSwiglu && c0 + i < ch.n) ? P.row_scale[ch.p0 + c0 + i] : 1.f;
         __syncwarp();
         tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(t * NMAX + c0), v);
         tmem_wait_ld();
@@ -590,10 +594,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
             const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
             if (n < ch.n && (r & 1) == 0) {
-              const float rsc = P.row_scale[p];
+              const float rsc = rs8[i];
               const float gv = acc * gsc * rsc;
               const float uv = other * o_gsc * rsc;
-              const float hv = gv / (1.f + expf(-gv)) * uv * kHScaleInv;
+              const float hv = gv / (1.f + __expf(-gv)) * uv * kHScaleInv;
               const int f = m * 64 + (r >> 1);
               P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
             }
@@ -742,7 +746,7 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
     g += v.x;
     u += v.y;
   }
-  const float hv = g / (1.f + expf(-g)) * u * kHScaleInv;
+  const float hv = g / (1.f + __expf(-g)) * u * kHScaleInv;
   h16[i] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
 }
 

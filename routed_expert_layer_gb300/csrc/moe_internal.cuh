@@ -26,6 +26,12 @@ __device__ __forceinline__ void pdl_entry() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Whether launch_pdl adds the attribute: set for the duration of a decode-sized forward
+// by the host thread that enqueues it. At prefill sizes launch latency is noise, and a
+// dependent grid that becomes resident early only holds SM slots, so there the kernels
+// are launched plainly (griddepcontrol.wait is then a no-op).
+extern thread_local bool g_launch_pdl;
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args&&... args) {
@@ -40,7 +46,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_launch_pdl ? 1 : 0;
     return cudaLaunchKernelExC(&cfg, (const void*)kernel, p);
   }(std::forward<Args>(args)...);
 }

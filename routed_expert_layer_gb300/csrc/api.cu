@@ -221,8 +221,16 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   const RouterTcPlan rp = router_tc_plan(sh, T, ctx->sm_count);
   CUtensorMap mx;
   if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)sh.H, (uint32_t)rp.nt, true)) return MOE_ERR_CUDA;
-  if (launch_router_tc(sh, rp, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool small = T <= kRouteSmallT;  // E <= 1024 and k <= 32 hold for every supported shape
+  if (launch_router_tc(sh, rp, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s, !small) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageRouter);
+  if (small) {  // reduce, select and permute in one CTA
+    if (tm) tm->begin(kStageSelect);
+    if (launch_route_small(sh, ctx->L, ctx->ws, T, rp.S, nmax, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (tm) tm->end(kStageSelect);
+    ctx->launches += 2;
+    return MOE_OK;
+  }
   if (tm) tm->begin(kStageSelect);
   if (launch_select(sh, ctx->ws.logits, ctx->ws.idx, ctx->ws.w, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageSelect);

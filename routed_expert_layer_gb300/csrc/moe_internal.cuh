@@ -198,8 +198,13 @@ cudaError_t launch_router_reduce(const Shape& sh, const DeviceLayer& L, const Wo
 RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count);
 cudaError_t launch_router_split(const Shape& sh, const float* W, uint16_t* w3, cudaStream_t s);
 cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx,
-                             const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s);
+                             const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s,
+                             bool reduce = true);
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s);
+// S1 reduce + S2 + S3 of a batch of at most kRouteSmallT tokens in one launch (E <= 1024, k <= 32).
+constexpr int kRouteSmallT = 32;
+cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
+                               cudaStream_t s);
 // nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
                            int nmax = 0);

@@ -154,13 +154,9 @@ __device__ __forceinline__ unsigned long long lane_best(const unsigned long long
   return t[0];
 }
 
-__global__ void select_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
-                              int T, int E, int k) {
-  pdl_entry();
-  const int tok = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (tok >= T) return;
-  const float* l = logits + (size_t)tok * E;
+// Top-k of one token's logits l[0..E) by one warp; lanes j < k write idx_out[j], w_out[j].
+__device__ __forceinline__ void select_token(const float* __restrict__ l, int E, int k, int lane,
+                                             int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
   unsigned long long keys[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -191,9 +187,18 @@ __global__ void select_kernel(const float* __restrict__ logits, int32_t* __restr
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
   if (lane < k) {
-    idx[(size_t)tok * k + lane] = my_e;
-    w[(size_t)tok * k + lane] = p / sum;
+    idx_out[lane] = my_e;
+    w_out[lane] = p / sum;
   }
+}
+
+__global__ void select_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
+                              int T, int E, int k) {
+  pdl_entry();
+  const int tok = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= T) return;
+  select_token(logits + (size_t)tok * E, E, k, lane, idx + (size_t)tok * k, w + (size_t)tok * k);
 }
 
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s) {
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(256) perm_masks_kernel(const int32_t* __restri
   }
 }
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, at most 1024).
 __device__ int block_exclusive_scan(int v, int* total) {
   __shared__ int warp_sums[32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -245,7 +250,7 @@ __device__ int block_exclusive_scan(int v, int* total) {
   if (lane == 31) warp_sums[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    int ws = warp_sums[lane];
+    int ws = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
     int wi = ws;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -330,6 +335,141 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint3
   perm[p] = t;
   slot[p] = j;
   inv[i] = p;
+}
+
+// ---- small batches: S1..S3 after the router GEMM in one CTA -------------------------------
+
+// For T <= 32 tokens (one 32-token chunk) and E <= 1024 one CTA of 512 threads does what
+// router_reduce_kernel, select_kernel, perm_masks_kernel, perm_scan_kernel and
+// perm_scatter_kernel do, with the same arithmetic in the same order: the router's K-split
+// partial sums are added in ascending split order and the bias added last, the top-k is
+// select_token, and the routes are counted, scanned and scattered exactly as for one
+// chunk of tokens (thread i owns experts i and i + 512). One launch instead of five on
+// the latency-bound small-batch path.
+constexpr int kRouteSmallThreads = 512;
+
+__global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
+    const float* __restrict__ part, const float* __restrict__ bias, int S, float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ active, int32_t* __restrict__ meta, int32_t* __restrict__ perm, int32_t* __restrict__ slot,
+    int32_t* __restrict__ inv, TcChunk* __restrict__ chunks, int nmax, int chunk_cap, uint32_t* __restrict__ err, int T,
+    int E, int k) {
+  pdl_entry();
+  constexpr int NT = kRouteSmallThreads;
+  __shared__ uint32_t mask[2 * NT];  // bit t of mask[e]: token t chose expert e
+  __shared__ int off_s[2 * NT];
+  __shared__ int totals[6];
+  __shared__ int max_rows;
+  const int tid = threadIdx.x;
+  const size_t n = (size_t)T * E;
+  // four logits per thread at a time and the split loop unrolled, so that up to 16 loads
+  // are in flight while each sum still runs over the splits in ascending order
+  for (size_t i0 = tid; i0 < n; i0 += 4 * (size_t)NT) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {
+      float v[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const size_t i = i0 + (size_t)q * NT;
+          v[u][q] = i < n ? part[(size_t)(s + u) * n + i] : 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] += v[u][q];
+    }
+    for (; s < S; ++s)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const size_t i = i0 + (size_t)q * NT;
+        if (i < n) acc[q] += part[(size_t)s * n + i];
+      }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const size_t i = i0 + (size_t)q * NT;
+      if (i < n) logits[i] = acc[q] + bias[i % E];
+    }
+  }
+  mask[tid] = 0u;
+  mask[tid + NT] = 0u;
+  if (tid == 0) max_rows = 0;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int t = warp; t < T; t += NT / 32)
+    select_token(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
+  __syncthreads();
+  for (int i = tid; i < T * k; i += NT) {
+    const int e = idx[i];
+    if (e < 0 || e >= E) {
+      atomicOr(err, kErrExpertRange);
+      continue;
+    }
+    atomicOr(&mask[e], 1u << (i / k));
+  }
+  __syncthreads();
+  const int e0 = tid, e1 = tid + NT;
+  const int run0 = e0 < E ? __popc(mask[e0]) : 0;
+  const int run1 = e1 < E ? __popc(mask[e1]) : 0;
+  if (e0 < E) counts[e0] = run0;
+  if (e1 < E) counts[e1] = run1;
+  const int rmax = max(run0, run1);
+  if (rmax > 0) atomicMax(&max_rows, rmax);
+  const int off0 = block_exclusive_scan(run0, &totals[0]);
+  const int off1 = block_exclusive_scan(run1, &totals[1]) + totals[0];
+  const int pos0 = block_exclusive_scan(run0 > 0 ? 1 : 0, &totals[2]);
+  const int pos1 = block_exclusive_scan(run1 > 0 ? 1 : 0, &totals[3]) + totals[2];
+  off_s[e0] = off0;
+  off_s[e1] = off1;
+  if (e0 < E) {
+    offsets[e0] = off0;
+    if (run0 > 0) active[pos0] = e0;
+  }
+  if (e1 < E) {
+    offsets[e1] = off1;
+    if (run1 > 0) active[pos1] = e1;
+  }
+  if (tid == 0) {
+    offsets[E] = totals[0] + totals[1];
+    meta[0] = totals[2] + totals[3];
+    meta[1] = max_rows;
+  }
+  if (chunks) {  // each expert's rows cut into runs of at most nmax (uniform branch)
+    const int nch0 = (run0 + nmax - 1) / nmax, nch1 = (run1 + nmax - 1) / nmax;
+    const int cb0 = block_exclusive_scan(nch0, &totals[4]);
+    const int cb1 = block_exclusive_scan(nch1, &totals[5]) + totals[4];
+    for (int j = 0; j < nch0; ++j)
+      if (cb0 + j < chunk_cap) chunks[cb0 + j] = TcChunk{e0, off0 + j * nmax, min(nmax, run0 - j * nmax), 0};
+    for (int j = 0; j < nch1; ++j)
+      if (cb1 + j < chunk_cap) chunks[cb1 + j] = TcChunk{e1, off1 + j * nmax, min(nmax, run1 - j * nmax), 0};
+    if (tid == 0) {
+      const int tot = totals[4] + totals[5];
+      if (tot > chunk_cap) atomicOr(err, kErrCountOverflow);
+      meta[2] = min(tot, chunk_cap);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < T * k; i += NT) {
+    const int t = i / k, j = i - t * k;
+    const int ei = idx[i];
+    if (ei < 0 || ei >= E) {
+      inv[i] = -1;
+      continue;
+    }
+    const int p = off_s[ei] + __popc(mask[ei] & ((1u << t) - 1u));
+    perm[p] = t;
+    slot[p] = j;
+    inv[i] = p;
+  }
+}
+
+cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
+                               cudaStream_t s) {
+  return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteSmallThreads), 0, s, ws.router_part, L.router_bias, S, ws.logits,
+                    ws.idx, ws.w, ws.counts, ws.offsets, ws.active, ws.meta, ws.perm, ws.slot, ws.inv,
+                    nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err, T, sh.E, sh.k);
 }
 
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,

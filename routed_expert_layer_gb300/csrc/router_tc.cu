@@ -268,7 +268,7 @@ static cudaError_t launch_router_tc_t(const CUtensorMap& mw, const CUtensorMap& 
 }
 
 cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx,
-                             const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s) {
+                             const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s, bool reduce) {
   RouterTcParams P;
   P.T = T;
   P.E = sh.E;
@@ -281,7 +281,7 @@ cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUte
   P.part = ws.router_part;
   P.err = ws.err;
   cudaError_t e = pl.small ? launch_router_tc_t<64>(mw, mx, P, pl.grid, s) : launch_router_tc_t<256>(mw, mx, P, pl.grid, s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !reduce) return e;
   return launch_router_reduce(sh, L, ws, T, pl.S, s);
 }
 

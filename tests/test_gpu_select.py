@@ -87,3 +87,34 @@ def test_select_is_deterministic(ctxs):
     moe.debug_select(l, perm=b)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("H,I,E,k,T", [(256, 128, 32, 4, 1), (256, 128, 32, 4, 32), (512, 256, 64, 8, 7),
+                                       (256, 128, 896, 16, 1), (256, 128, 896, 16, 8), (256, 128, 896, 16, 32),
+                                       (256, 128, 1024, 32, 17), (256, 128, 896, 16, 33)])
+def test_small_batch_route_matches_general_path(H, I, E, k, T):
+    """Batches of at most 32 tokens are routed by one fused kernel (reduce, select and
+    permute in one CTA). Given the logits it produced, the general select and permute
+    kernels must give bit-identical results; T = 33 takes the general path on both sides."""
+    import torch
+    import routed_expert_layer_gb300 as rel
+    moe = rel.MoeLayer(H, I, E, k, 64)
+    try:
+        moe.load(synth.layer(H, I, E, seed_weights=11, seed_router=12))
+        x = torch.from_numpy(synth.x_bf16(900 + T, T, H).view(np.int16)).cuda()
+        names = ("idx", "w", "offsets", "perm", "slot", "inv")
+        shapes = dict(idx=((T, k), torch.int32), w=((T, k), torch.float32), offsets=((E + 1,), torch.int32),
+                      perm=((T * k,), torch.int32), slot=((T * k,), torch.int32), inv=((T * k,), torch.int32))
+        a = {n: torch.empty(*shapes[n][0], dtype=shapes[n][1], device="cuda") for n in names}
+        b = {n: torch.empty(*shapes[n][0], dtype=shapes[n][1], device="cuda") for n in names}
+        logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+        moe.debug_route(x, logits=logits, **a)
+        moe.debug_select(logits, **b)
+        torch.cuda.synchronize()
+        for n in names:
+            assert torch.equal(a[n], b[n]), n
+        ref_idx, _ = oracle.select(logits.cpu().numpy(), k)
+        assert np.array_equal(a["idx"].cpu().numpy(), ref_idx)
+        assert moe.get_error() == 0
+    finally:
+        moe.close()

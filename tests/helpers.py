@@ -17,6 +17,11 @@ SHAPES = {
     "tiny": dict(H=256, I=128, E=32, k=4),
     "mid": dict(H=512, I=256, E=64, k=8),
     "k3": dict(H=7168, I=1536, E=896, k=16),
+    # degenerate routings: one expert (the layer is one SwiGLU MLP) and k = E = 32 (every
+    # token uses every expert: a dense softmax mixture); the widest supported row, H = 14336
+    "single": dict(H=256, I=128, E=1, k=1),
+    "dense": dict(H=256, I=128, E=32, k=32),
+    "wide": dict(H=14336, I=256, E=16, k=4),
 }
 
 

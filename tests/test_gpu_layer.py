@@ -215,3 +215,15 @@ def test_profile_hooks_under_graph_capture(mid):
     torch.cuda.synchronize()
     prof = mid.profile_end()
     assert prof["gateup"][1] == 1 and prof["gateup"][0] > 0 and prof["down"][0] > 0
+
+
+@pytest.mark.parametrize("name,T", [("single", 1), ("single", 9), ("dense", 3), ("dense", 40), ("wide", 5),
+                                    ("wide", 33)])
+def test_degenerate_and_extreme_shapes(name, T):
+    """E = k = 1 (one SwiGLU MLP), k = E = 32 (every expert for every token) and the
+    widest supported hidden size (H = 14336), through the whole layer."""
+    m = make(name, 64)
+    try:
+        run_case(m, name, T, 600 + T)
+    finally:
+        m.close()

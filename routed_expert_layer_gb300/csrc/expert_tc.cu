@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
+      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's tensor scale
 #pragma unroll
       for (int n = 0; n < NMAX; ++n) {
         if (n >= N) break;
@@ -352,7 +353,6 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         if (P.mode == kTcModeSwiglu) {
           // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
           const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-          const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
           if (n < ch.n && (r & 1) == 0) {
             const float rsc = P.row_scale[p];
             const float gv = acc * gsc * rsc;
@@ -576,6 +576,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const TcChunk ch = P.chunks[ci];
       const int N = ((ch.n + 15) / 16) * 16;
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
+      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's tensor scale
       for (int c0 = hh * (N / 2); c0 < (hh + 1) * (N / 2); c0 += 8) {
         uint32_t v[8];
         float rs8[8];  // row scales of the 8 rows, loaded ahead of the accumulator read
@@ -592,7 +593,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           const float acc = __uint_as_float(v[i]);
           if (P.mode == kTcModeSwiglu) {
             const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-            const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);
             if (n < ch.n && (r & 1) == 0) {
               const float rsc = rs8[i];
               const float gv = acc * gsc * rsc;
@@ -785,15 +785,33 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
     for (int j = 0; j < 32; ++j)
       if (j < k) acc_f16x8(u[j], wj[j], acc);
   } else {
-    for (int j = 0; j < k; ++j) {
-      const int p = inv[(size_t)t * k + j];
-      if (p < 0) continue;
-      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < S; ++s)
-        acc_f16x8(reinterpret_cast<const uint4*>(y + (size_t)s * slice + (size_t)p * H)[c8], 1.f, v);
-      const float wj = w[(size_t)t * k + j] * kYScale;
+    // eight routes at a time, so that their loads of one split are in flight together;
+    // each route's splits are still added in ascending order before it is weighted
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int pj[8];
+      float v[8][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+      for (int q = 0; q < 8; ++q) {
+        pj[q] = j0 + q < k ? inv[(size_t)t * k + j0 + q] : -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[q][i] = 0.f;
+      }
+      for (int s = 0; s < S; ++s) {
+        uint4 u[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          u[q] = pj[q] < 0 ? make_uint4(0, 0, 0, 0)
+                           : reinterpret_cast<const uint4*>(y + (size_t)s * slice + (size_t)pj[q] * H)[c8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc_f16x8(u[q], 1.f, v[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (pj[q] < 0) continue;
+        const float wj = w[(size_t)t * k + j0 + q] * kYScale;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[q][i], acc[i]);
+      }
     }
   }
   uint4 packed;

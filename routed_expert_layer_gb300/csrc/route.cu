@@ -362,35 +362,65 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   __shared__ int max_rows;
   const int tid = threadIdx.x;
   const size_t n = (size_t)T * E;
-  // four logits per thread at a time and the split loop unrolled, so that up to 16 loads
-  // are in flight while each sum still runs over the splits in ascending order
-  for (size_t i0 = tid; i0 < n; i0 += 4 * (size_t)NT) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
-      float v[4][4];
+  // Sixteen-byte loads of four adjacent logits' partial sums, four groups per thread
+  // and the split loop unrolled by four, so that up to sixteen 16-B loads per thread are
+  // in flight; each logit's sum still runs over the splits in ascending order.
+  if ((n & 3) == 0) {
+    const size_t n4 = n / 4;
+    const float4* part4 = reinterpret_cast<const float4*>(part);
+    for (size_t g0 = tid; g0 < n4; g0 += 4 * (size_t)NT) {
+      float4 acc[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      int s = 0;
+      for (; s + 4 <= S; s += 4) {
+        float4 v[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const size_t g = g0 + (size_t)q * NT;
+            v[u][q] = g < n4 ? part4[(size_t)(s + u) * n4 + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[q].x += v[u][q].x;
+            acc[q].y += v[u][q].y;
+            acc[q].z += v[u][q].z;
+            acc[q].w += v[u][q].w;
+          }
+      }
+      for (; s < S; ++s)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const size_t i = i0 + (size_t)q * NT;
-          v[u][q] = i < n ? part[(size_t)(s + u) * n + i] : 0.f;
+          const size_t g = g0 + (size_t)q * NT;
+          if (g < n4) {
+            const float4 v = part4[(size_t)s * n4 + g];
+            acc[q].x += v.x;
+            acc[q].y += v.y;
+            acc[q].z += v.z;
+            acc[q].w += v.w;
+          }
         }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] += v[u][q];
-    }
-    for (; s < S; ++s)
-#pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const size_t i = i0 + (size_t)q * NT;
-        if (i < n) acc[q] += part[(size_t)s * n + i];
+        const size_t g = g0 + (size_t)q * NT;
+        if (g < n4) {
+          const size_t i = 4 * g;
+          logits[i + 0] = acc[q].x + bias[(i + 0) % E];
+          logits[i + 1] = acc[q].y + bias[(i + 1) % E];
+          logits[i + 2] = acc[q].z + bias[(i + 2) % E];
+          logits[i + 3] = acc[q].w + bias[(i + 3) % E];
+        }
       }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const size_t i = i0 + (size_t)q * NT;
-      if (i < n) logits[i] = acc[q] + bias[i % E];
+    }
+  } else {
+    for (size_t i = tid; i < n; i += NT) {
+      float acc = 0.f;
+      for (int s = 0; s < S; ++s) acc += part[(size_t)s * n + i];
+      logits[i] = acc + bias[i % E];
     }
   }
   mask[tid] = 0u;

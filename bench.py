@@ -169,18 +169,24 @@ def cpu_baseline_bounded(L, batches, min_s=10.0):
 
 def run_reference(args, rank, world):
     """Reference arm: the oracle timed as it stands on the host cores. Each step is
-    the oracle on a window of 4 tokens of the decode batch (the window moves each
-    step), so K steps stay within a few minutes."""
+    the oracle on a window of up to 4 tokens of the decode batch (the window moves each
+    step), sized from a first untimed call so that K + W steps take a few minutes."""
     if rank != 0:
         return
     import synth
     L = make_layer()
     x = synth.x_bf16(3, args.T, K3["H"])
-    n = args.cpu_sample or 4
-    n = min(n, args.T)
+    n = min(args.cpu_sample or 4, args.T)
+
     def window(i):
         s0 = (i * n) % max(1, args.T - n + 1)
         return x[s0:s0 + n]
+    if not args.cpu_sample:
+        # size the window so that all K + W steps take about two and a half minutes
+        t0 = time.perf_counter()
+        cpu_baseline(L, window(0), n)
+        per_token = (time.perf_counter() - t0) / n
+        n = max(1, min(n, int(150.0 / (max(1, args.steps + args.warmup) * per_token))))
     for i in range(args.warmup):
         cpu_baseline(L, window(i), n)
     t0 = time.perf_counter()

@@ -12,7 +12,8 @@
  *     FP8 scale per 16 values plus a per-expert global scale.
  *   - "Serving Kimi-K3 ... with 8xB300 GPUs", section "The model, as the serving
  *     system sees it": 3 matrices per expert, 4-bit E2M1 values two per byte.
- *   - SemiAnalysis essay on MoE serving (Chinese translation), sections 4 and 15:
+ *   - "Computation and Data Movement for Inference" (Chinese translation of an essay
+ *     on MoE serving), sections 4 and 15:
  *     route records are sorted by expert so one weight load serves a bucket, then
  *     expert outputs are restored to token order, weighted and merged.
  * The pages leave open the score function, tie rule, activation and global-scale

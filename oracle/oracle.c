@@ -22,7 +22,8 @@
  *                  experts per layer.
  *   S3 permute     route records sorted by expert (stable in token order):
  *                  counts, exclusive offsets, perm[p] = token, slot[p] = j,
- *                  inv[t*k + j] = p. SemiAnalysis essay (Chinese translation),
+ *                  inv[t*k + j] = p. "Computation and Data Movement for
+ *                  Inference" (Chinese translation),
  *                  section 4 (the prefill MoE flow: sort or queue route records
  *                  by expert so one weight load serves a whole bucket) and
  *                  section 15 (records are built, counted, permuted, and
@@ -37,7 +38,7 @@
  *   S5 down        y[p] = w[perm[p]][slot[p]] * (W_d h[p]).
  *   S6 combine     out[t] = sum over j ascending of y[inv[t*k + j]]: expert
  *                  outputs restored to token order, weighted and merged
- *                  (SemiAnalysis essay, section 4).
+ *                  ("Computation and Data Movement for Inference", section 4).
  *
  * Formats (decoded here from their definitions, not from any library):
  *   E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; codes 0..7 are

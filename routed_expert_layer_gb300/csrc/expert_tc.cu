@@ -1,8 +1,9 @@
 // Expert FFN on the 5th-generation tensor cores (S4 gate/up + SwiGLU, S5 down, S6 combine).
 //
 // Every touched expert's bucket of routed rows is one grouped-GEMM problem
-// (SemiAnalysis essay, section 4: one expert weight load serves the whole bucket;
-// section 15: AI ~ 2nW / (B_W + n B_A + B_O) grows with the bucket size n). The
+// ("Computation and Data Movement for Inference", section 4: one expert weight load
+// serves the whole bucket; section 15: the arithmetic intensity 2nW / (B_W + n B_A +
+// B_O) grows with the bucket size n). The
 // weights are NVFP4 ("Kimi-K3 NVFP4 station eight sparks", section "What has to be
 // built"): E2M1 codes with an E4M3 scale per 16 values along K and an fp32 scale
 // per tensor.
@@ -21,10 +22,11 @@
 //   D accumulates in fp32 in tensor memory; the epilogue applies the tensor and
 //       row scales and either the SwiGLU (gate/up rows are interleaved in the tile)
 //       or writes fp32 partial sums of a K split.
-// Warp roles: warp 0 issues TMA, warp 1 issues MMAs (one thread), the other warps
-// dequantise and run the epilogue (warp w may only touch TMEM lanes 32*(w%4)..).
-// Both variants run one persistent CTA per SM over a device-built list of work items
-// (expert, row range, M tile(s), K split).
+// Warp roles: warp 0 issues the copies, one thread of each MMA warp issues MMAs, the
+// other warps dequantise and run the epilogue (warp w may only touch TMEM lanes
+// 32*(w%4)..). The kernels are persistent over a device-built list of work items
+// (expert, row range, M tile(s), K split): the decode variant with two CTAs per SM and
+// two MMA warps each, the prefill variant with one CTA per SM.
 #include <cuda.h>
 
 #include <algorithm>

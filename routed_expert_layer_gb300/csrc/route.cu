@@ -8,8 +8,9 @@
 // S2: 16 of 896 experts per token ("Serving Kimi-K3 ... with 8xB300 GPUs", section
 //     "The model, as the serving system sees it"). Order: logit descending, expert
 //     index ascending, -0 == +0; made total by a 64-bit key so the result is unique.
-// S3: route records sorted by expert, stable in token order (SemiAnalysis essay,
-//     sections 4 and 15: build records, count, permute, later restore token order).
+// S3: route records sorted by expert, stable in token order ("Computation and Data
+//     Movement for Inference", sections 4 and 15: build records, count, permute, later
+//     restore token order).
 #include "moe_internal.cuh"
 
 namespace moe {

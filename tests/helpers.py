@@ -22,6 +22,8 @@ SHAPES = {
     "single": dict(H=256, I=128, E=1, k=1),
     "dense": dict(H=256, I=128, E=32, k=32),
     "wide": dict(H=14336, I=256, E=16, k=4),
+    # the pages' own expert geometry (latent experts d = 3584, f = 3072; same bytes per expert)
+    "latent": dict(H=3584, I=3072, E=896, k=16),
 }
 
 

@@ -56,20 +56,21 @@ def check_permutation_properties(r, T, E, k):
         assert np.all(np.diff(perm[offs[e]:offs[e + 1]]) > 0)
 
 
-def run_k3(moe, T, zipf=False):
-    L = layer("k3", zipf)
-    x = synth.x_bf16(3 + T, T, K3["H"])
+def run_k3(moe, T, zipf=False, name="k3"):
+    s = SHAPES[name]
+    L = layer(name, zipf)
+    x = synth.x_bf16(3 + T, T, s["H"])
     out = gpu_forward(moe, x)
-    r = gpu_route(moe, x, K3["E"], K3["k"])
-    check_permutation_properties(r, T, K3["E"], K3["k"])
+    r = gpu_route(moe, x, s["E"], s["k"])
+    check_permutation_properties(r, T, s["E"], s["k"])
     rows = sample_rows(T)
-    ref, ref_idx, ref_w, ref_logits = oracle.moe_tokens(oracle.Layer(L), x[rows], K3["k"])
+    ref, ref_idx, ref_w, ref_logits = oracle.moe_tokens(oracle.Layer(L), x[rows], s["k"])
     ref_abs = oracle.router_abs(x[rows], L.router_w)
-    ties = check_routing(r["logits"][rows], r["idx"][rows], ref_logits, ref_abs, ref_idx, K3["k"])
+    ties = check_routing(r["logits"][rows], r["idx"][rows], ref_logits, ref_abs, ref_idx, s["k"])
     ratio = check_output(out[rows], ref, ~ties)
     assert moe.get_error() == 0
     counts = np.diff(r["offsets"])
-    print(f"K3 T={T} zipf={zipf}: touched={int((counts > 0).sum())} max_rows={int(counts.max())} "
+    print(f"{name.upper()} T={T} zipf={zipf}: touched={int((counts > 0).sum())} max_rows={int(counts.max())} "
           f"err/rms={ratio:.3e} near_ties={int(ties.sum())}")
 
 
@@ -81,3 +82,20 @@ def test_k3_uniform(k3, T):
 @pytest.mark.parametrize("T", [64, 4096])
 def test_k3_zipf(k3_zipf, T):
     run_k3(k3_zipf, T, zipf=True)
+
+
+@pytest.fixture(scope="module")
+def latent():
+    import routed_expert_layer_gb300 as rel
+    s = SHAPES["latent"]
+    m = rel.MoeLayer(s["H"], s["I"], s["E"], s["k"], 4096)
+    m.load(layer("latent"))
+    yield m
+    m.close()
+
+
+@pytest.mark.parametrize("T", [1, 53, 4096])
+def test_latent_expert_shape(latent, T):
+    """The pages' own expert geometry (d = 3584, f = 3072, 896 experts, top-16): the same
+    kernels, shape-parametric, decode and prefill."""
+    run_k3(latent, T, name="latent")

@@ -107,8 +107,13 @@ MOE_API int moe_load_layer(moe_ctx* ctx, const moe_layer_host* layer);
 /* The layer on T tokens: out[t][:] = sum_j w[t][j] * FFN_{idx[t][j]}(x[t][:]).
  *   x    device bf16 [T][H], row-major, 16-byte aligned
  *   out  device bf16 [T][H], 16-byte aligned, must not overlap x
- * Asynchronous on `stream`; allocates nothing; does not synchronise the host.
- * T == 0 returns MOE_OK and enqueues nothing; T > max_tokens is an error. */
+ * Asynchronous on `stream`; allocates nothing; does not synchronise the host; may be
+ * captured in a CUDA graph. T == 0 returns MOE_OK and enqueues nothing; T > max_tokens
+ * is an error. At decode sizes (T*k/E < 8) the kernels are launched with programmatic
+ * stream serialisation and the last one lets the next kernel on the stream launch
+ * before it has finished: a following kernel that is itself launched with that
+ * attribute must wait on its grid dependency (griddepcontrol.wait) before reading out;
+ * kernels launched without it, copies and events wait for completion as usual. */
 MOE_API int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T);
 
 /* The same through HOST buffers: copies x (host bf16 [T][H]) to the device,

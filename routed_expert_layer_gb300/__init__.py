@@ -35,7 +35,7 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
-KERNEL_REV = {"router": "tc3-1", "select": "warp-4", "permute": "mask-4", "gather": "f16-2",
+KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-5", "gather": "f16-2",
               "gateup": "tc-9", "down": "tc-9", "combine": "f32-3"}
 
 

@@ -154,6 +154,7 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.x_stage = cv.take<uint16_t>(T * H);
   w.out_stage = cv.take<uint16_t>(T * H);
   w.err = cv.take<uint32_t>(1);
+  w.ticket = cv.take<uint32_t>(1);
   w.xg = cv.take<uint16_t>(T * k * H);
   w.row_scale = cv.take<float>(T * k);
   w.h16 = cv.take<uint16_t>(T * k * I);
@@ -221,7 +222,8 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   const RouterTcPlan rp = router_tc_plan(sh, T, ctx->sm_count);
   CUtensorMap mx;
   if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)sh.H, (uint32_t)rp.nt, true)) return MOE_ERR_CUDA;
-  const bool small = T <= kRouteSmallT;  // E <= 1024 and k <= 32 hold for every supported shape
+  // E <= 1024 and k <= 32 hold for every supported shape
+  const bool small = T <= kRouteSmallT && sh.E % 4 == 0 && rp.S <= 64;
   if (launch_router_tc(sh, rp, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s, !small) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageRouter);
   if (small) {  // reduce, select and permute in one CTA
@@ -365,6 +367,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   workspace_layout(*cfg, ctx->sm_count, &ctx->ws, (char*)ctx->ws_mem);
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
   if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(ctx->ws.ticket, 0, sizeof(uint32_t)) != cudaSuccess ||
       !make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
       !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false) ||
       !make_tmap_16(&ctx->tmap_x64, ctx->ws.xg, rows, cfg->hidden, 64, false) ||

@@ -171,6 +171,7 @@ struct Workspace {
   uint16_t* x_stage = nullptr;    // [T][H] for moe_forward_host
   uint16_t* out_stage = nullptr;  // [T][H]
   uint32_t* err = nullptr;        // device error word
+  uint32_t* ticket = nullptr;     // CTAs finished in route_small_kernel (zero between calls)
   // tensor-core path
   uint16_t* xg = nullptr;         // [T*k][H] f16 activation rows in routed order
   float* row_scale = nullptr;     // [T*k] 2^-sigma of each row of xg
@@ -201,7 +202,8 @@ cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUte
                              const DeviceLayer& L, const Workspace& ws, int T, cudaStream_t s,
                              bool reduce = true);
 cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, float* w, int T, cudaStream_t s);
-// S1 reduce + S2 + S3 of a batch of at most kRouteSmallT tokens in one launch (E <= 1024, k <= 32).
+// S1 reduce + S2 + S3 of a batch of at most kRouteSmallT tokens in one launch (E <= 1024,
+// E % 4 == 0, k <= 32, router K splits <= 64).
 constexpr int kRouteSmallT = 32;
 cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
                                cudaStream_t s);

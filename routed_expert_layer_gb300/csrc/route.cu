@@ -156,13 +156,16 @@ __device__ __forceinline__ unsigned long long lane_best(const unsigned long long
 }
 
 // Top-k of one token's logits l[0..E) by one warp; lanes j < k write idx_out[j], w_out[j].
+// L2 = true reads the logits at L2 (they were written by other CTAs of the same grid).
+template <bool L2 = false>
 __device__ __forceinline__ void select_token(const float* __restrict__ l, int E, int k, int lane,
                                              int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
   unsigned long long keys[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int e = lane + 32 * i;
-    keys[i] = (e < E) ? (((unsigned long long)ordered_bits(l[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e))
+    const float le = e < E ? (L2 ? __ldcg(l + e) : l[e]) : 0.f;
+    keys[i] = (e < E) ? (((unsigned long long)ordered_bits(le) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e))
                       : 0ull;
   }
   unsigned long long best = lane_best(keys);
@@ -181,7 +184,7 @@ __device__ __forceinline__ void select_token(const float* __restrict__ l, int E,
       best = lane_best(keys);
     }
   }
-  const float v = (lane < k) ? l[my_e] : 0.f;
+  const float v = (lane < k) ? (L2 ? __ldcg(l + my_e) : l[my_e]) : 0.f;
   const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
   float p = (lane < k) ? expf(v - m0) : 0.f;
   float sum = p;
@@ -340,97 +343,71 @@ __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint3
 
 // ---- small batches: S1..S3 after the router GEMM in one CTA -------------------------------
 
-// For T <= 32 tokens (one 32-token chunk) and E <= 1024 one CTA of 512 threads does what
+// For T <= 32 tokens (one 32-token chunk) and E <= 1024 this kernel does what
 // router_reduce_kernel, select_kernel, perm_masks_kernel, perm_scan_kernel and
-// perm_scatter_kernel do, with the same arithmetic in the same order: the router's K-split
-// partial sums are added in ascending split order and the bias added last, the top-k is
-// select_token, and the routes are counted, scanned and scattered exactly as for one
-// chunk of tokens (thread i owns experts i and i + 512). One launch instead of five on
-// the latency-bound small-batch path.
+// perm_scatter_kernel do, with the same arithmetic in the same order, in one launch:
+//  1. every CTA adds the router's K-split partial sums of 128 logits in ascending split
+//     order and adds the bias last (the partial sums are first staged in shared memory,
+//     so each thread has all its loads in flight at once);
+//  2. the CTA that finishes last (a ticket taken after a device-scope fence; no CTA
+//     ever waits for another) takes the top-k of every token with select_token, then
+//     counts, scans and scatters the routes exactly as for one chunk of 32 tokens
+//     (thread i owns experts i and i + 512), and returns the ticket to zero.
 constexpr int kRouteSmallThreads = 512;
+constexpr int kRouteSmallGroups = 32;  // float4 groups of logits per CTA in step 1
+constexpr int kRouteSmallMaxS = 64;    // router K splits staged in shared memory
 
 __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
     const float* __restrict__ part, const float* __restrict__ bias, int S, float* __restrict__ logits,
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ active, int32_t* __restrict__ meta, int32_t* __restrict__ perm, int32_t* __restrict__ slot,
-    int32_t* __restrict__ inv, TcChunk* __restrict__ chunks, int nmax, int chunk_cap, uint32_t* __restrict__ err, int T,
-    int E, int k) {
+    int32_t* __restrict__ inv, TcChunk* __restrict__ chunks, int nmax, int chunk_cap, uint32_t* __restrict__ err,
+    uint32_t* __restrict__ ticket, int T, int E, int k) {
   pdl_entry();
-  constexpr int NT = kRouteSmallThreads;
+  constexpr int NT = kRouteSmallThreads, G = kRouteSmallGroups;
+  __shared__ float4 stage[kRouteSmallMaxS][G];
   __shared__ uint32_t mask[2 * NT];  // bit t of mask[e]: token t chose expert e
   __shared__ int off_s[2 * NT];
   __shared__ int totals[6];
   __shared__ int max_rows;
+  __shared__ int last;
   const int tid = threadIdx.x;
-  const size_t n = (size_t)T * E;
-  // Sixteen-byte loads of four adjacent logits' partial sums, four groups per thread
-  // and the split loop unrolled by four, so that up to sixteen 16-B loads per thread are
-  // in flight; each logit's sum still runs over the splits in ascending order.
-  if ((n & 3) == 0) {
-    const size_t n4 = n / 4;
-    const float4* part4 = reinterpret_cast<const float4*>(part);
-    for (size_t g0 = tid; g0 < n4; g0 += 4 * (size_t)NT) {
-      float4 acc[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      int s = 0;
-      for (; s + 4 <= S; s += 4) {
-        float4 v[4][4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const size_t g = g0 + (size_t)q * NT;
-            v[u][q] = g < n4 ? part4[(size_t)(s + u) * n4 + g] : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[q].x += v[u][q].x;
-            acc[q].y += v[u][q].y;
-            acc[q].z += v[u][q].z;
-            acc[q].w += v[u][q].w;
-          }
-      }
-      for (; s < S; ++s)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const size_t g = g0 + (size_t)q * NT;
-          if (g < n4) {
-            const float4 v = part4[(size_t)s * n4 + g];
-            acc[q].x += v.x;
-            acc[q].y += v.y;
-            acc[q].z += v.z;
-            acc[q].w += v.w;
-          }
-        }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const size_t g = g0 + (size_t)q * NT;
-        if (g < n4) {
-          const size_t i = 4 * g;
-          logits[i + 0] = acc[q].x + bias[(i + 0) % E];
-          logits[i + 1] = acc[q].y + bias[(i + 1) % E];
-          logits[i + 2] = acc[q].z + bias[(i + 2) % E];
-          logits[i + 3] = acc[q].w + bias[(i + 3) % E];
-        }
-      }
-    }
-  } else {
-    for (size_t i = tid; i < n; i += NT) {
+  const size_t n = (size_t)T * E, n4 = n / 4;  // E % 4 == 0 (launcher)
+  // 1. logits of this CTA's groups
+  const float4* part4 = reinterpret_cast<const float4*>(part);
+  const size_t g0 = (size_t)blockIdx.x * G;
+  for (int i = tid; i < S * G; i += NT) {
+    const int s = i / G, gl = i - s * G;
+    if (g0 + gl < n4) stage[s][gl] = part4[(size_t)s * n4 + g0 + gl];
+  }
+  __syncthreads();
+  if (tid < 4 * G) {
+    const int gl = tid >> 2, c = tid & 3;
+    if (g0 + gl < n4) {
+      const float* st = reinterpret_cast<const float*>(&stage[0][gl]) + c;
       float acc = 0.f;
-      for (int s = 0; s < S; ++s) acc += part[(size_t)s * n + i];
+      for (int s = 0; s < S; ++s) acc += st[(size_t)s * G * 4];
+      const size_t i = 4 * (g0 + gl) + c;
       logits[i] = acc + bias[i % E];
     }
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // 2. the last CTA: selection and permutation of all T tokens
   mask[tid] = 0u;
   mask[tid + NT] = 0u;
-  if (tid == 0) max_rows = 0;
+  if (tid == 0) {
+    max_rows = 0;
+    *ticket = 0u;  // every CTA has taken its ticket
+  }
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
   for (int t = warp; t < T; t += NT / 32)
-    select_token(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
+    select_token<true>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
   __syncthreads();
   for (int i = tid; i < T * k; i += NT) {
     const int e = idx[i];
@@ -498,9 +475,12 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
 
 cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
                                cudaStream_t s) {
-  return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteSmallThreads), 0, s, ws.router_part, L.router_bias, S, ws.logits,
-                    ws.idx, ws.w, ws.counts, ws.offsets, ws.active, ws.meta, ws.perm, ws.slot, ws.inv,
-                    nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err, T, sh.E, sh.k);
+  const size_t n4 = (size_t)T * sh.E / 4;
+  const unsigned grid = (unsigned)((n4 + kRouteSmallGroups - 1) / kRouteSmallGroups);
+  return launch_pdl(route_small_kernel, dim3(grid), dim3(kRouteSmallThreads), 0, s, ws.router_part, L.router_bias, S,
+                    ws.logits, ws.idx, ws.w, ws.counts, ws.offsets, ws.active, ws.meta, ws.perm, ws.slot, ws.inv,
+                    nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err, ws.ticket, T, sh.E,
+                    sh.k);
 }
 
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,

@@ -249,6 +249,36 @@ def time_config(moe, xs, steps, warmup, stream, profile=False):
     return a.elapsed_time(b) / steps, prof, int(per_forward * steps)
 
 
+def replay_distribution(moe, xs, stream, n=64):
+    """Per-forward device times of n graph replays (CUDA events around each replay on
+    the launching stream), outside the timed region: p10 / p50 / p90 in ms. None if
+    anything goes wrong (this is a side measurement, never the headline)."""
+    try:
+        import torch
+        outs = [torch.empty_like(x) for x in xs]
+        graphs = []
+        for i in range(len(xs)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                moe.forward(xs[i], outs[i], stream)
+            graphs.append(g)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(len(graphs)):
+                graphs[i].replay()
+            for i in range(n):
+                evs[i][0].record(stream)
+                graphs[i % len(graphs)].replay()
+                evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        t = np.array([a.elapsed_time(b) for a, b in evs])
+        del graphs
+        return {"n": n, "p10_ms": round(float(np.percentile(t, 10)), 5), "p50_ms": round(float(np.percentile(t, 50)), 5),
+                "p90_ms": round(float(np.percentile(t, 90)), 5)}
+    except Exception as e:  # noqa: BLE001
+        return {"error": str(e)[:200]}
+
+
 def profile_run(args):
     """Forwards of a K3-shaped layer (H=7168, I=1536, k=16) with --experts experts at --T
     tokens: a small case of the same kernels for ncu captures."""
@@ -313,6 +343,7 @@ def main():
     ms, prof, n_launch = time_config(moe, xs, args.steps, args.warmup, stream, profile=True)
     clocks = sampler.stop()
     ms_all, value = job_throughput(ms, T, world, "cuda")
+    replays = replay_distribution(moe, xs, stream) if rank == 0 else None
 
     # ---- end to end through the host-buffer entry point --------------------------------
     xh = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
@@ -381,6 +412,7 @@ def main():
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": int(gu_bytes),
                          "dominant_stage": dom},
             "stage_ms": {k_: round(v, 5) for k_, v in stages.items()},
+            "replay_ms": replays,
             "gpu_launches": int(n_launch),
             "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": T * K3["H"] * 2,
                     "d2h_bytes_per_step": T * K3["H"] * 2},

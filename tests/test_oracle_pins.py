@@ -307,3 +307,33 @@ def test_pins_catch_planted_mistakes():
     rms = np.sqrt(np.mean(out ** 2))
     for name, wrong in mistakes.items():
         assert np.max(np.abs(wrong - out)) > 0.1 * rms, name
+
+
+# ---- the oracle's result does not depend on its thread count --------------------------------
+
+_THREADS_SNIPPET = """
+import sys, numpy as np
+sys.path.insert(0, {root!r})
+import oracle, synth
+L = synth.layer(256, 128, 32, seed_weights=41, seed_router=42)
+x = synth.x_bf16(43, 19, 256)
+out, idx, w, logits = oracle.moe_forward(oracle.Layer(L), x, 4)
+sys.stdout.buffer.write(out.tobytes() + idx.tobytes() + w.tobytes() + logits.tobytes())
+"""
+
+
+def test_oracle_is_independent_of_thread_count():
+    """Every output's reduction order is fixed, so one OpenMP thread and several give
+    the same bytes (the oracle's timing runs use all host cores)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = _THREADS_SNIPPET.format(root=root)
+    outs = []
+    for n in ("1", "4"):
+        env = dict(os.environ, OMP_NUM_THREADS=n)
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, env=env, timeout=300)
+        assert r.returncode == 0, r.stderr.decode()[-2000:]
+        outs.append(r.stdout)
+    assert len(outs[0]) > 0 and outs[0] == outs[1]

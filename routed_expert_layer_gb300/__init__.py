@@ -149,6 +149,26 @@ def _dptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _rows(t, H: int, what: str, cuda: bool) -> int:
+    """Check that t is a contiguous [T][H] array of 2-byte elements (a CUDA tensor when
+    cuda, else a numpy array or a host torch tensor) and return T. The C entry points
+    take plain pointers, so this is where a wrong shape is caught."""
+    shape = tuple(t.shape)
+    if len(shape) != 2 or shape[1] != H:
+        raise ValueError(f"{what}: expected shape [T][{H}], got {list(shape)}")
+    if isinstance(t, np.ndarray):
+        if cuda:
+            raise ValueError(f"{what}: expected a CUDA tensor, got a numpy array")
+        if t.itemsize != 2 or not t.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{what}: expected contiguous 2-byte elements")
+        return shape[0]
+    if t.element_size() != 2 or not t.is_contiguous():
+        raise ValueError(f"{what}: expected contiguous 2-byte elements")
+    if t.is_cuda != cuda:
+        raise ValueError(f"{what}: expected a {'CUDA' if cuda else 'host'} tensor")
+    return shape[0]
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -176,7 +196,14 @@ class MoeLayer:
     def load(self, layer) -> None:
         """layer: object with numpy arrays gu_codes [E][2I][H/2], gu_scales, gu_global [E][2],
         dn_codes [E][H][I/2], dn_scales, dn_global [E], router_w [H][E], router_bias [E] or None."""
-        E = self.cfg.n_experts
+        E, H, I = self.cfg.n_experts, self.cfg.hidden, self.cfg.inter
+        expect = {"gu_codes": (E, 2 * I, H // 2), "gu_scales": (E, 2 * I, H // 16), "gu_global": (E, 2),
+                  "dn_codes": (E, H, I // 2), "dn_scales": (E, H, I // 16), "dn_global": (E,), "router_w": (H, E)}
+        for name, shape in expect.items():  # the library reads these sizes through plain pointers
+            if tuple(np.shape(getattr(layer, name))) != shape:
+                raise ValueError(f"{name}: expected shape {list(shape)}, got {list(np.shape(getattr(layer, name)))}")
+        if layer.router_bias is not None and tuple(np.shape(layer.router_bias)) != (E,):
+            raise ValueError(f"router_bias: expected shape [{E}]")
         keep = []
 
         def arr(a, dtype):
@@ -202,12 +229,16 @@ class MoeLayer:
 
     def forward(self, x, out, stream=None) -> None:
         """x, out: CUDA tensors of bf16 [T][H] (any dtype with 2-byte elements)."""
-        T = x.shape[0]
+        T = _rows(x, self.H, "x", True)
+        if _rows(out, self.H, "out", True) != T:
+            raise ValueError("out: expected as many rows as x")
         _check(lib().moe_forward(self.ctx, _stream(stream), _dptr(x), _dptr(out), T), "moe_forward")
 
     def forward_host(self, x_host, out_host, stream=None) -> None:
         """x_host, out_host: host buffers (numpy uint16 or pinned torch tensors) of [T][H] bf16."""
-        T = x_host.shape[0]
+        T = _rows(x_host, self.H, "x_host", False)
+        if _rows(out_host, self.H, "out_host", False) != T:
+            raise ValueError("out_host: expected as many rows as x_host")
         xp = x_host.ctypes.data if isinstance(x_host, np.ndarray) else x_host.data_ptr()
         op = out_host.ctypes.data if isinstance(out_host, np.ndarray) else out_host.data_ptr()
         _check(lib().moe_forward_host(self.ctx, _stream(stream), ctypes.c_void_p(xp), ctypes.c_void_p(op), T),
@@ -215,6 +246,7 @@ class MoeLayer:
 
     def debug_route(self, x, logits=None, idx=None, w=None, offsets=None, perm=None, slot=None, inv=None,
                     stream=None):
+        _rows(x, self.H, "x", True)
         _check(lib().moe_debug_route(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(logits), _dptr(idx),
                                      _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
                "moe_debug_route")
@@ -225,6 +257,7 @@ class MoeLayer:
                "moe_debug_select")
 
     def debug_experts(self, x, h=None, y=None, stream=None):
+        _rows(x, self.H, "x", True)
         _check(lib().moe_debug_experts(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(h), _dptr(y)),
                "moe_debug_experts")
 

@@ -86,3 +86,44 @@ def test_profile_stage_names(L):
     names = [L.moe_profile_stage_name(i).decode() for i in range(n)]
     assert names[:3] == ["router", "select", "permute"] and "combine" in names
     assert L.moe_profile_stage_name(n) == b""
+
+
+def test_binding_checks_token_arrays():
+    """The binding checks shapes before it hands plain pointers to the library."""
+    import numpy as np
+    import torch
+    import routed_expert_layer_gb300 as rel
+    assert rel._rows(torch.zeros(3, 256, dtype=torch.int16), 256, "x", False) == 3
+    assert rel._rows(np.zeros((0, 256), dtype=np.uint16), 256, "x", False) == 0
+    bad = [(torch.zeros(3, 128, dtype=torch.int16), False),          # wrong H
+           (torch.zeros(3, 256, dtype=torch.float32), False),        # 4-byte elements
+           (torch.zeros(256, 3, dtype=torch.int16).t(), False),      # not contiguous
+           (torch.zeros(3, 256, dtype=torch.int16), True),           # host tensor where CUDA is needed
+           (np.zeros((3, 256), dtype=np.uint16), True),              # numpy where CUDA is needed
+           (np.zeros((3, 256), dtype=np.float32), False),
+           (torch.zeros(768, dtype=torch.int16), False)]             # not 2-D
+    for t, cuda in bad:
+        with pytest.raises(ValueError):
+            rel._rows(t, 256, "x", cuda)
+
+
+def test_binding_checks_layer_shapes():
+    """load() rejects weight arrays whose shapes do not match the context's config before
+    the library reads them (checked on a stand-in object, no device needed)."""
+    import dataclasses
+    import numpy as np
+    import synth
+    import routed_expert_layer_gb300 as rel
+    L = synth.layer(256, 128, 32, seed_weights=1, seed_router=2)
+
+    class Stub(rel.MoeLayer):  # skips moe_create: only the host-side checks run
+        def __init__(self):
+            self.cfg = rel.Config(256, 128, 32, 4, 8, 0)
+            self.ctx = None
+
+    for name in ("gu_codes", "dn_scales", "router_w"):
+        bad = dataclasses.replace(L, **{name: np.zeros((1, 2), dtype=getattr(L, name).dtype)})
+        with pytest.raises(ValueError):
+            Stub().load(bad)
+    with pytest.raises(ValueError):
+        Stub().load(dataclasses.replace(L, router_bias=np.zeros(31, dtype=np.float32)))

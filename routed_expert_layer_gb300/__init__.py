@@ -31,7 +31,7 @@ MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_DEVICE_FLAG = -4, -5, -6
 EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "moe_destroy", "moe_status_str",
             "moe_get_error", "moe_debug_route", "moe_debug_select", "moe_debug_experts", "moe_profile_stages",
             "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count",
-            "moe_route_noalloc"]
+            "moe_route_noalloc", "moe_plan"]
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
@@ -116,6 +116,7 @@ def lib():
         L.moe_profile_end.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32), i32]
         L.moe_device_bytes.restype = ctypes.c_int64
         L.moe_device_bytes.argtypes = [vp]
+        L.moe_plan.argtypes = [ctypes.POINTER(Config), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
         L.moe_launch_count.restype = ctypes.c_int64
         L.moe_launch_count.argtypes = [vp]
         L.moe_route_noalloc.argtypes = [vp, p, p, p, i32, i32, i32, i32, p, p, p, p, p, p]
@@ -174,6 +175,18 @@ def _stream(stream):
         import torch
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+PLAN_FIELDS = ("prefill", "rows_per_item", "gateup_splits", "down_splits", "gemm_ctas", "router_splits",
+               "router_ctas", "fused_routing", "chunk_capacity", "workspace_bytes")
+
+
+def plan(hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, sm_count: int, T: int) -> dict:
+    """The launch plan moe_forward uses for T tokens (host only, no GPU needed)."""
+    cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0)
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(lib().moe_plan(ctypes.byref(cfg), sm_count, T, out), "moe_plan")
+    return {k: int(v) for k, v in zip(PLAN_FIELDS, out)}
 
 
 class MoeLayer:

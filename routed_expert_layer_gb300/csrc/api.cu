@@ -222,8 +222,7 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   const RouterTcPlan rp = router_tc_plan(sh, T, ctx->sm_count);
   CUtensorMap mx;
   if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)sh.H, (uint32_t)rp.nt, true)) return MOE_ERR_CUDA;
-  // E <= 1024 and k <= 32 hold for every supported shape
-  const bool small = T <= kRouteSmallT && sh.E % 4 == 0 && rp.S <= 64;
+  const bool small = route_small_ok(sh, T, rp.S);
   if (launch_router_tc(sh, rp, ctx->tmap_w3, mx, ctx->L, ctx->ws, T, s, !small) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageRouter);
   if (small) {  // reduce, select and permute in one CTA
@@ -609,6 +608,28 @@ int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t n) {
     }
   ctx->prof_max = 0;
   ctx->prof_calls = 0;
+  return MOE_OK;
+}
+
+int moe_plan(const moe_config* cfg, int32_t sm_count, int32_t T, int64_t* plan) {
+  const int st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!plan || sm_count < 1 || T < 1 || T > cfg->max_tokens) return MOE_ERR_INVALID_ARG;
+  const Shape sh{cfg->hidden, cfg->inter, cfg->n_experts, cfg->top_k};
+  const TcPlan pl = tc_plan(sh, T, sm_count);
+  const RouterTcPlan rp = router_tc_plan(sh, T, sm_count);
+  Workspace w;
+  const size_t bytes = workspace_layout(*cfg, sm_count, &w, nullptr);
+  plan[0] = pl.prefill ? 1 : 0;
+  plan[1] = pl.nmax;
+  plan[2] = pl.S1;
+  plan[3] = pl.S2;
+  plan[4] = pl.grid;
+  plan[5] = rp.S;
+  plan[6] = rp.grid;
+  plan[7] = route_small_ok(sh, T, rp.S) ? 1 : 0;
+  plan[8] = w.chunk_cap;
+  plan[9] = (int64_t)bytes;
   return MOE_OK;
 }
 

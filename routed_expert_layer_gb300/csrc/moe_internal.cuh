@@ -205,6 +205,9 @@ cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, fl
 // S1 reduce + S2 + S3 of a batch of at most kRouteSmallT tokens in one launch (E <= 1024,
 // E % 4 == 0, k <= 32, router K splits <= 64).
 constexpr int kRouteSmallT = 32;
+inline bool route_small_ok(const Shape& sh, int T, int router_splits) {
+  return T <= kRouteSmallT && sh.E <= 1024 && sh.E % 4 == 0 && sh.k <= 32 && router_splits <= 64;
+}
 cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
                                cudaStream_t s);
 // nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).

@@ -127,3 +127,28 @@ def test_binding_checks_layer_shapes():
             Stub().load(bad)
     with pytest.raises(ValueError):
         Stub().load(dataclasses.replace(L, router_bias=np.zeros(31, dtype=np.float32)))
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/moe_gb300.h is a C header: a C99 translation unit that takes the address
+    of every declared entry point compiles without warnings (and so does C++)."""
+    import re
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    inc = os.path.join(root, "include")
+    text = open(os.path.join(inc, "moe_gb300.h")).read()
+    names = re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+    assert len(names) >= 18
+    src = tmp_path / "abi.c"
+    src.write_text('#include "moe_gb300.h"\n'
+                   "typedef void (*fn)(void);\n"
+                   "fn entry_points[] = {" + ", ".join(f"(fn){n}" for n in names) + "};\n")
+    for cc, std in (("gcc", "-std=c99"), ("g++", "-std=c++17")):
+        exe = shutil.which(cc)
+        if exe is None:
+            pytest.skip(f"{cc} not found")
+        lang = ["-x", "c++"] if cc == "g++" else []
+        r = subprocess.run([exe, *lang, std, "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(src), "-o",
+                            str(tmp_path / f"abi_{cc}.o")], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr

@@ -48,3 +48,14 @@ def test_reference_arm_other_ranks_print_nothing():
     with redirect_stdout(buf):
         bench.run_reference(args, 1, 2)
     assert buf.getvalue() == ""
+
+
+def test_roofline_constants_match_the_byte_census():
+    """The bench's per-expert byte counts are the page's census: 18,579,480 B per expert,
+    of which gate + up are two thirds of the codes and scales plus their two fp32 scales."""
+    import bench
+    H, I = 7168, 1536
+    assert bench.EXPERT_BYTES == 18_579_480
+    assert bench.GU_BYTES == 2 * I * H // 2 + 2 * I * H // 16 + 8 == 12_386_312
+    assert bench.DN_BYTES == H * I // 2 + H * I // 16 + 4 == 6_193_156
+    assert bench.GU_BYTES + bench.DN_BYTES == bench.EXPERT_BYTES

@@ -51,11 +51,13 @@ def test_reference_arm_other_ranks_print_nothing():
 
 
 def test_roofline_constants_match_the_byte_census():
-    """The bench's per-expert byte counts are the page's census: 18,579,480 B per expert,
-    of which gate + up are two thirds of the codes and scales plus their two fp32 scales."""
+    """The bench's per-expert byte counts follow the page's census of 18,579,480 B per
+    expert in 12 tensors (3 x codes, block scales, tensor scale, input scale): gate + up
+    are two thirds of the codes and block scales plus their two tensor scales, down the
+    rest plus one; the three 4-byte input scales are not read with 16-bit activations."""
     import bench
     H, I = 7168, 1536
     assert bench.EXPERT_BYTES == 18_579_480
     assert bench.GU_BYTES == 2 * I * H // 2 + 2 * I * H // 16 + 8 == 12_386_312
     assert bench.DN_BYTES == H * I // 2 + H * I // 16 + 4 == 6_193_156
-    assert bench.GU_BYTES + bench.DN_BYTES == bench.EXPERT_BYTES
+    assert bench.GU_BYTES + bench.DN_BYTES + 3 * 4 == bench.EXPERT_BYTES

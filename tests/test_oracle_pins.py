@@ -134,6 +134,24 @@ def test_router_vs_numpy_matmul():
     assert np.allclose(got, ref, rtol=0, atol=1e-12)
 
 
+def test_router_abs_vs_numpy_and_triangle_inequality():
+    """sum_h |x_h W[h, e]| (the scale every routing check's logit bound is measured in)
+    against numpy fp64 |x| @ |W|; it bounds |logit| (triangle inequality), with equality
+    when every product is non-negative; a signed sum (the plausible slip) fails the pin."""
+    x = synth.x_bf16(5, 6, 256)
+    W = synth.router(2, 256, 32)
+    got = oracle.router_abs(x, W)
+    ref = np.abs(bf16_lib(x)) @ np.abs(W.astype(np.float64))
+    assert np.allclose(got, ref, rtol=1e-13, atol=0)
+    logits = oracle.router_logits(x, W)
+    assert np.all(np.abs(logits) <= got * (1 + 1e-12))
+    xp = x & np.uint16(0x7FFF)  # clear the bf16 sign bits: every product is >= 0
+    Wp = np.abs(W)
+    assert np.allclose(oracle.router_abs(xp, Wp), oracle.router_logits(xp, Wp), rtol=1e-13, atol=0)
+    signed = np.abs(bf16_lib(x) @ W.astype(np.float64))
+    assert np.max(np.abs(signed - got) / got) > 0.5
+
+
 # ---- P-C select ----------------------------------------------------------------------------
 
 def _brute_select(logits, k):

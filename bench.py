@@ -18,6 +18,7 @@ replicas); value = tokens of all ranks / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -131,9 +132,25 @@ class ClockSampler:
 
 
 def make_layer(zipf=False):
+    """The K3 layer (weights seed 1, router seed 2); zipf=True adds the Zipf(1.1) router
+    bias over a seeded permutation of the experts (seed 4)."""
     import synth
-    L = synth.layer(K3["H"], K3["I"], K3["E"], seed_weights=1, seed_router=2)
-    return L
+    return synth.layer(K3["H"], K3["I"], K3["E"], seed_weights=1, seed_router=2, zipf_seed=4 if zipf else None)
+
+
+def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2):
+    """Device time per forward at one batch size (graph replays over the rotating batches
+    xs) with the touched experts, the largest bucket and the roofline fractions."""
+    Ts = xs[0].shape[0]
+    msw, _, _ = time_config(moe, xs, reps, warmup, stream)
+    tch = [touched(moe, x, K3["E"], K3["k"]) for x in xs]
+    dsw = float(np.mean([t[0] for t in tch]))
+    byts = dsw * EXPERT_BYTES
+    flops = 6.0 * Ts * K3["k"] * K3["H"] * K3["I"]
+    return {"ms": round(msw, 4), "tokens_per_s": round(Ts / (msw * 1e-3), 1), "touched_experts": dsw,
+            "largest_bucket": int(max(t[1] for t in tch)), "replays": reps, "batches": len(xs),
+            "hbm_frac": round(byts / (msw * 1e-3) / 1e9 / hbm, 4),
+            "tensor_frac": round(flops / (msw * 1e-3) / 1e12 / bf16, 4)}
 
 
 def cpu_baseline(L, x_bits, n_tokens):
@@ -377,17 +394,26 @@ def main():
 
     sweep = {}
     if not args.no_sweep and rank == 0:
+        sweep_sampler = ClockSampler(gpu_id)
         for Ts in (1, 8, 64, 128, 256, 2048, 4096, 8192):
-            xsw = [torch.from_numpy(synth.x_bf16(500 + i + Ts, Ts, K3["H"]).view(np.int16)).cuda() for i in range(2)]
-            reps = 30 if Ts <= 256 else 3
-            msw, _, _ = time_config(moe, xsw, reps, 2, stream)
-            dsw = touched(moe, xsw[0], K3["E"], K3["k"])[0]
-            byts = dsw * EXPERT_BYTES
-            flops = 6.0 * Ts * K3["k"] * K3["H"] * K3["I"]
-            sweep[f"T{Ts}"] = {"ms": round(msw, 4), "tokens_per_s": round(Ts / (msw * 1e-3), 1),
-                               "touched_experts": dsw,
-                               "hbm_frac": round(byts / (msw * 1e-3) / 1e9 / hbm, 4),
-                               "tensor_frac": round(flops / (msw * 1e-3) / 1e12 / bf16, 4)}
+            nb = 4 if Ts >= 2048 else 2
+            xsw = [torch.from_numpy(synth.x_bf16(500 + i + Ts, Ts, K3["H"]).view(np.int16)).cuda()
+                   for i in range(nb)]
+            sweep[f"T{Ts}"] = sweep_point(moe, xsw, stream, hbm, bf16, reps=30 if Ts <= 256 else 20)
+            del xsw
+        # Zipf(1.1)-skewed routing: the same experts, a router bias making a few experts hot
+        zl = dataclasses.replace(L, router_bias=synth.zipf_bias(4, K3["E"], 1.1))
+        mz = rel.MoeLayer(K3["H"], K3["I"], K3["E"], K3["k"], 4096, device=local)
+        mz.load(zl)
+        for Ts in (64, 4096):
+            nb = 4 if Ts >= 2048 else 2
+            xsw = [torch.from_numpy(synth.x_bf16(700 + i + Ts, Ts, K3["H"]).view(np.int16)).cuda()
+                   for i in range(nb)]
+            sweep[f"zipf_T{Ts}"] = sweep_point(mz, xsw, stream, hbm, bf16, reps=30 if Ts <= 256 else 20)
+            sweep[f"zipf_T{Ts}"]["vs_uniform"] = round(sweep[f"T{Ts}"]["ms"] / sweep[f"zipf_T{Ts}"]["ms"], 4)
+            del xsw
+        mz.close()
+        sweep["clocks"] = sweep_sampler.stop()
 
     cb = None
     if rank == 0:

@@ -129,7 +129,11 @@ MOE_API const char* moe_status_str(int status);
 
 /* Read and clear the device error word (synchronises the device). Returns
  * MOE_OK if no kernel raised it, MOE_ERR_DEVICE_FLAG otherwise; *bits (may be
- * NULL) receives the raw word: 1 = expert id out of range, 2 = row count overflow. */
+ * NULL) receives the raw word: 1 = expert id out of range, 2 = row count overflow,
+ * 4 = a bounded wait inside a GEMM gave up (the kernel stopped early), 8 = an f16
+ * intermediate (SwiGLU or down-projection value, stored in normalised units) was
+ * beyond the f16 range or not finite; it is stored as the conversion gives it (an
+ * infinity or NaN, never clamped), so the output shows it too. */
 MOE_API int moe_get_error(moe_ctx* ctx, uint32_t* bits);
 
 /* ---- inspection hooks (tests and benchmarking) ----------------------------- */
@@ -185,15 +189,21 @@ MOE_API int moe_profile_end(moe_ctx* ctx, float* ms, int32_t* launches, int32_t 
  *   router_w   device fp32 [H][E]; router_bias device fp32 [E] or NULL
  *   idx, w, offsets, perm, slot, inv: device outputs, caller-allocated, laid out
  *              as for moe_debug_route (all required)
+ *   err        device uint32 or NULL: when given, the routing kernels OR the error
+ *              bits of moe_get_error into it (1 = expert id out of range); the caller
+ *              clears it and reads it after the stream has finished
  * Limits: H % 64 == 0, 1 <= k <= 32, k <= E <= MOE_NOALLOC_MAX_EXPERTS,
  * 1 <= T <= MOE_NOALLOC_MAX_TOKENS; larger sizes return MOE_ERR_UNSUPPORTED.
  * The first call on a device looks up the scratch's device address (make it
- * before any stream capture). All calls share the one array: calls whose GPU work
- * overlaps (unordered streams) race and corrupt each other's results. The device
- * error word of this path is internal and cleared on every call. */
+ * before any stream capture); the address belongs to the device's primary context,
+ * so only that context (the one the CUDA runtime uses) is supported. All calls share
+ * the one array: calls whose GPU work overlaps (unordered streams) race and corrupt
+ * each other's results. The logits come from an fp32 SIMT router and may differ from
+ * moe_forward's tensor-core logits in the last bits, so two experts whose logits are
+ * that close may be ordered differently. */
 MOE_API int moe_route_noalloc(void* stream, const void* x, const float* router_w, const float* router_bias,
                               int32_t H, int32_t E, int32_t k, int32_t T, int32_t* idx, float* w, int32_t* offsets,
-                              int32_t* perm, int32_t* slot, int32_t* inv);
+                              int32_t* perm, int32_t* slot, int32_t* inv, uint32_t* err);
 
 /* Number of kernels this context has enqueued so far (all calls that run kernels). */
 MOE_API int64_t moe_launch_count(const moe_ctx* ctx);

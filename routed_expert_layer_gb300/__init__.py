@@ -35,8 +35,8 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
-KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-5", "gather": "f16-2",
-              "gateup": "tc-9", "down": "tc-9", "combine": "f32-3"}
+KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-5", "gather": "f16-3",
+              "gateup": "tc-10", "down": "tc-10", "combine": "f32-4"}
 
 
 def _nvcc() -> str:
@@ -119,18 +119,48 @@ def lib():
         L.moe_plan.argtypes = [ctypes.POINTER(Config), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]
         L.moe_launch_count.restype = ctypes.c_int64
         L.moe_launch_count.argtypes = [vp]
-        L.moe_route_noalloc.argtypes = [vp, p, p, p, i32, i32, i32, i32, p, p, p, p, p, p]
+        L.moe_route_noalloc.argtypes = [vp, p, p, p, i32, i32, i32, i32, p, p, p, p, p, p, p]
         _lib = L
     return _lib
 
 
-def route_noalloc(x, router_w, router_bias, k, idx, w, offsets, perm, slot, inv, stream=None) -> None:
-    """Routing without any device allocation (see moe_route_noalloc in the header):
-    every argument is a CUDA tensor on the current device; outputs are caller-allocated."""
+def route_noalloc(x, router_w, router_bias, k, idx, w, offsets, perm, slot, inv, err=None, stream=None) -> None:
+    """Routing without any device allocation (see moe_route_noalloc in the header).
+    Every argument is a contiguous CUDA tensor on the current device; the outputs are
+    caller-allocated: idx int32 [T][k], w float32 [T][k], offsets int32 [E+1], perm, slot,
+    inv int32 [T*k]; err (optional) a uint32/int32 word the kernels OR their error bits
+    into. The C entry point only sees plain pointers, so every size is checked here."""
+    import torch
+    if x.dim() != 2 or x.element_size() != 2:
+        raise ValueError("x: expected [T][H] with 2-byte (bf16) elements")
     T, H = x.shape
+    if router_w.dim() != 2 or router_w.shape[0] != H or router_w.dtype != torch.float32:
+        raise ValueError(f"router_w: expected float32 [{H}][E], got {router_w.dtype} {list(router_w.shape)}")
     E = router_w.shape[1]
+    expect = {"idx": (idx, (T, k), torch.int32), "w": (w, (T, k), torch.float32),
+              "offsets": (offsets, (E + 1,), torch.int32), "perm": (perm, (T * k,), torch.int32),
+              "slot": (slot, (T * k,), torch.int32), "inv": (inv, (T * k,), torch.int32)}
+    if router_bias is not None:
+        expect["router_bias"] = (router_bias, (E,), torch.float32)
+    if err is not None:
+        if err.numel() != 1 or err.element_size() != 4:
+            raise ValueError("err: expected one 4-byte word")
+        expect["err"] = (err, tuple(err.shape), err.dtype)
+    tensors = {"x": (x, (T, H), x.dtype), "router_w": (router_w, (H, E), torch.float32), **expect}
+    for name, (t, shape, dtype) in tensors.items():
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name}: expected {dtype} {list(shape)}, got {t.dtype} {list(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name}: expected a CUDA tensor")
+    dev = torch.cuda.current_device()
+    for name, (t, _, _) in tensors.items():
+        if t.device.index != dev:
+            raise ValueError(f"{name}: expected a tensor on the current device cuda:{dev}, got {t.device}")
     _check(lib().moe_route_noalloc(_stream(stream), _dptr(x), _dptr(router_w), _dptr(router_bias), H, E, k, T,
-                                   _dptr(idx), _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
+                                   _dptr(idx), _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv),
+                                   _dptr(err)),
            "moe_route_noalloc")
 
 

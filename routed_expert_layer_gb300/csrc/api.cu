@@ -156,7 +156,8 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.err = cv.take<uint32_t>(1);
   w.ticket = cv.take<uint32_t>(1);
   w.xg = cv.take<uint16_t>(T * k * H);
-  w.row_scale = cv.take<float>(T * k);
+  w.gate_f = cv.take<float>(T * k);
+  w.comb_f = cv.take<float>(T * k);
   w.h16 = cv.take<uint16_t>(T * k * I);
   w.part1 = cv.take<float>(part1);
   w.ytc = cv.take<uint16_t>(ytc);
@@ -167,7 +168,9 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
 }
 
 struct WeightPtrs {
-  float *router_w, *router_bias, *gu_global, *dn_global;
+  float *router_w, *router_bias, *gu_global, *dn_global, *gu_norm, *dn_norm;
+  int32_t* norm_exp;
+  uint32_t* scale_max;
   uint16_t* w3;
   uint8_t *gu_tc, *dn_tc;
 };
@@ -180,6 +183,10 @@ size_t weights_layout(const moe_config& c, WeightPtrs* p, char* base) {
   w.router_bias = cv.take<float>(E);
   w.gu_global = cv.take<float>(2 * E);
   w.dn_global = cv.take<float>(E);
+  w.gu_norm = cv.take<float>(2 * E);
+  w.dn_norm = cv.take<float>(E);
+  w.norm_exp = cv.take<int32_t>(4 * E);
+  w.scale_max = cv.take<uint32_t>(3 * E);
   w.w3 = cv.take<uint16_t>(((E + 127) / 128) * 128 * 3 * H);
   w.gu_tc = cv.take<uint8_t>(E * 2 * I * H * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
   w.dn_tc = cv.take<uint8_t>(E * H * I * 9 / 16);
@@ -249,7 +256,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   const Workspace& ws = ctx->ws;
   const int rows = T * sh.k;
   if (tm) tm->begin(kStagePrep);
-  if (launch_gather_x(sh, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gather_x(sh, ctx->L, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePrep);
 
   TcGemmParams P1;
@@ -259,11 +266,10 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P1.S = pl.S1;
   P1.chunks = ws.chunks;
   P1.n_chunks = ws.meta + 2;
-  P1.gscale = ctx->L.gu_global;
+  P1.gscale = ctx->L.gu_norm;
   P1.gstride = 2;
   P1.gsel = 1;
-  P1.row_scale = ws.row_scale;
-  P1.post_scale = 1.f;
+  P1.gate_f = ws.gate_f;
   P1.mode = pl.S1 == 1 ? kTcModeSwiglu : kTcModePartial;
   P1.out = ws.part1;
   P1.out_slice = (size_t)rows * 2 * sh.I;
@@ -289,11 +295,10 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P2.S = pl.S2;
   P2.chunks = ws.chunks;
   P2.n_chunks = ws.meta + 2;
-  P2.gscale = ctx->L.dn_global;
+  P2.gscale = ctx->L.dn_norm;
   P2.gstride = 1;
   P2.gsel = 0;
-  P2.row_scale = nullptr;
-  P2.post_scale = kHScale / kYScale;  // undo h's 2^-8, store y at 2^-8
+  P2.gate_f = nullptr;
   P2.mode = kTcModeOutF16;
   P2.out16 = ws.ytc;
   P2.out_slice = (size_t)rows * sh.H;
@@ -408,6 +413,9 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   ctx->L.router_w3 = W.w3;
   ctx->L.gu_global = W.gu_global;
   ctx->L.dn_global = W.dn_global;
+  ctx->L.gu_norm = W.gu_norm;
+  ctx->L.dn_norm = W.dn_norm;
+  ctx->L.norm_exp = W.norm_exp;
   ctx->L.gu_tc = W.gu_tc;
   ctx->L.dn_tc = W.dn_tc;
   const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
@@ -428,7 +436,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
              ? cudaMemcpy(W.router_bias, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice)
              : cudaMemset(W.router_bias, 0, E * sizeof(float))) != cudaSuccess ||
         cudaMemcpy(W.gu_global, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(W.dn_global, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaMemcpy(W.dn_global, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(W.scale_max, 0, 3 * E * sizeof(uint32_t)) != cudaSuccess) {
       st = MOE_ERR_CUDA;
       break;
     }
@@ -450,11 +459,14 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
           cudaMemcpyAsync(ss, lh->gu_scales[e], gu_sb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
           cudaMemcpyAsync(dc, lh->dn_codes[e], dn_cb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
           cudaMemcpyAsync(ds, lh->dn_scales[e], dn_sb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-          launch_repack_tc(ctx->sh, (int)e, sc, ss, dc, ds, W.gu_tc, W.dn_tc, s) != cudaSuccess) {
+          launch_repack_tc(ctx->sh, (int)e, sc, ss, dc, ds, W.gu_tc, W.dn_tc, s) != cudaSuccess ||
+          launch_scale_max(ctx->sh, (int)e, ss, ds, W.scale_max, s) != cudaSuccess) {
         st = MOE_ERR_CUDA;
         break;
       }
     }
+    if (st == MOE_OK && launch_norms(ctx->sh, W.scale_max, W.gu_norm, W.dn_norm, W.norm_exp, s) != cudaSuccess)
+      st = MOE_ERR_CUDA;
     if (st == MOE_OK && cudaStreamSynchronize(s) != cudaSuccess) st = MOE_ERR_CUDA;
   } while (0);
   cudaStreamDestroy(s);
@@ -563,7 +575,7 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   if (st != MOE_OK) return st;
   st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, pl, nullptr);
   if (st != MOE_OK) return st;
-  return launch_debug_hy(ctx->sh, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_debug_hy(ctx->sh, ctx->L, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_profile_stages(void) { return kNumStages; }

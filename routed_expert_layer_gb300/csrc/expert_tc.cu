@@ -103,6 +103,19 @@ __device__ __forceinline__ void dequant_unit(const uint4 cw, uint32_t s_lo, uint
   for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], s_hi);
 }
 
+// f16 of a normalised intermediate; a value beyond the f16 range or not finite is stored
+// as the conversion gives it (an infinity or NaN, never clamped) and raises the error word.
+__device__ __forceinline__ uint16_t f16_checked(float v, uint32_t* err) {
+  if (!(fabsf(v) <= 65504.f)) atomicOr(err, kErrF16Range);
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// SwiGLU in normalised units: gn, un normalised gate and up sums, gv the true gate
+// pre-activation; returns gn * un * sigmoid(gv) * 2^-6.
+__device__ __forceinline__ float swiglu_store(float gn, float un, float gv) {
+  return gn * un * kHStore / (1.f + __expf(-gv));
+}
+
 struct Ring {  // stage index and phase parity of a circular buffer of n slots
   int idx = 0;
   uint32_t ph = 0;
@@ -345,8 +358,8 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
-      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
-      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's tensor scale
+      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)];
+      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's normaliser
 #pragma unroll
       for (int n = 0; n < NMAX; ++n) {
         if (n >= N) break;
@@ -356,20 +369,17 @@ __global__ void __launch_bounds__(kThreadsD, 2)
           // rows 2f (gate) and 2f+1 (up) sit in adjacent lanes
           const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
           if (n < ch.n && (r & 1) == 0) {
-            const float rsc = P.row_scale[p];
-            const float gv = acc * gsc * rsc;
-            const float uv = other * o_gsc * rsc;
-            const float hv = gv / (1.f + __expf(-gv)) * uv * kHScaleInv;
+            const float gn = acc * gsc, un = other * o_gsc;
+            const float hv = swiglu_store(gn, un, gn * P.gate_f[p]);
             const int f = m * 64 + (r >> 1);
-            P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
+            P.h16[(size_t)p * P.I + f] = f16_checked(hv, P.err);
           }
         } else if (n < ch.n) {
-          const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
           const size_t o = (size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r;
           if (P.mode == kTcModeOutF16)
-            P.out16[o] = __half_as_ushort(__float2half_rn(fminf(fmaxf(acc * gsc * rsc, -65504.f), 65504.f)));
+            P.out16[o] = f16_checked(acc * gsc, P.err);
           else
-            P.out[o] = acc * gsc * rsc;
+            P.out[o] = acc * gsc;
         }
       }
     }
@@ -577,14 +587,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const int m = 2 * mp + t;
       const TcChunk ch = P.chunks[ci];
       const int N = ((ch.n + 15) / 16) * 16;
-      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)] * P.post_scale;
-      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's tensor scale
+      const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)];
+      const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's normaliser
       for (int c0 = hh * (N / 2); c0 < (hh + 1) * (N / 2); c0 += 8) {
         uint32_t v[8];
-        float rs8[8];  // row scales of the 8 rows, loaded ahead of the accumulator read
+        float rs8[8];  // gate factors of the 8 rows, loaded ahead of the accumulator read
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          rs8[i] = (P.mode == kTcModeSwiglu && c0 + i < ch.n) ? P.row_scale[ch.p0 + c0 + i] : 1.f;
+          rs8[i] = (P.mode == kTcModeSwiglu && c0 + i < ch.n) ? P.gate_f[ch.p0 + c0 + i] : 1.f;
         __syncwarp();
         tmem_ld8(tmem + lane_base + acc_col + (uint32_t)(t * NMAX + c0), v);
         tmem_wait_ld();
@@ -596,20 +606,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           if (P.mode == kTcModeSwiglu) {
             const float other = __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
             if (n < ch.n && (r & 1) == 0) {
-              const float rsc = rs8[i];
-              const float gv = acc * gsc * rsc;
-              const float uv = other * o_gsc * rsc;
-              const float hv = gv / (1.f + __expf(-gv)) * uv * kHScaleInv;
+              const float gn = acc * gsc, un = other * o_gsc;
+              const float hv = swiglu_store(gn, un, gn * rs8[i]);
               const int f = m * 64 + (r >> 1);
-              P.h16[(size_t)p * P.I + f] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
+              P.h16[(size_t)p * P.I + f] = f16_checked(hv, P.err);
             }
           } else if (n < ch.n) {
-            const float rsc = P.row_scale ? P.row_scale[p] : 1.f;
             const size_t o = (size_t)p * P.ldo + (size_t)m * 128 + r;
             if (P.mode == kTcModeOutF16)
-              P.out16[o] = __half_as_ushort(__float2half_rn(fminf(fmaxf(acc * gsc * rsc, -65504.f), 65504.f)));
+              P.out16[o] = f16_checked(acc * gsc, P.err);
             else
-              P.out[o] = acc * gsc * rsc;
+              P.out[o] = acc * gsc;
           }
         }
       }
@@ -629,14 +636,38 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
 // ---- activation rows in f16 ---------------------------------------------------------------
 
+// The two per-row factors of routed row p (expert e, activation scaled by 2^sigma) that
+// connect the normalised intermediates to true values (see moe_internal.cuh):
+//   gate_f[p] = g_gate * 2^(n_gate - sigma)
+//   comb_f[p] = g_down * g_gate * g_up * 2^(n_gate + n_up + n_down + 6 - 2 sigma)
+// The three tensor scales are split into mantissa and exponent first, so the product
+// over- or underflows only if the result itself does.
+struct RowFactors {
+  const int32_t* idx;
+  const float* gu_global;
+  const float* dn_global;
+  const int32_t* norm_exp;
+  float* gate_f;
+  float* comb_f;
+  __device__ __forceinline__ void write(int p, int e, int sigma) const {
+    const int32_t* n = norm_exp + 4 * e;
+    int a, b, c;
+    const float ma = frexpf(gu_global[2 * e], &a);
+    const float mb = frexpf(gu_global[2 * e + 1], &b);
+    const float mc = frexpf(dn_global[e], &c);
+    gate_f[p] = ldexpf(gu_global[2 * e], n[0] - sigma);
+    comb_f[p] = ldexpf(ma * mb * mc, a + b + c + n[0] + n[1] + n[2] + kHStoreExp - 2 * sigma);
+  }
+};
+
 // Token t's row, converted to f16 after scaling by 2^sigma so the row's largest
 // magnitude lands in [2^13, 2^14) (the conversion of bf16 values is then exact down to
-// 2^-28 of the row maximum), is written to each of its k routed rows inv[t*k+j];
-// row_scale[p] = 2^-sigma undoes the scaling in the epilogue. One warp per token:
-// the row is read once into registers (H <= 14336 -> at most 56 uint4 per lane).
+// 2^-28 of the row maximum), is written to each of its k routed rows inv[t*k+j], with
+// the row's factors. One warp per token: the row is read once into registers
+// (H <= 14336 -> at most 56 uint4 per lane).
 template <int MAXV>
 __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ inv,
-                                    uint16_t* __restrict__ xg, float* __restrict__ row_scale, int T, int H, int k) {
+                                    uint16_t* __restrict__ xg, const RowFactors rf, int T, int H, int k) {
   pdl_entry();
   const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -676,7 +707,7 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
   for (int j = 0; j < k; ++j) {
     const int p = inv[(size_t)t * k + j];
     if (p < 0) continue;
-    if (lane == 0) row_scale[p] = __int_as_float((127 - sigma) << 23);
+    if (lane == 0) rf.write(p, rf.idx[(size_t)t * k + j], sigma);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
@@ -691,7 +722,8 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
 // per-token kernel above, which reads each token row once instead of k times.
 template <int MAXV>
 __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
-                                       uint16_t* __restrict__ xg, float* __restrict__ row_scale, int rows, int H) {
+                                       const int32_t* __restrict__ slot, uint16_t* __restrict__ xg,
+                                       const RowFactors rf, int rows, int H, int k) {
   pdl_entry();
   const int p = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -717,7 +749,7 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
     sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
   }
   const float sc = __int_as_float((sigma + 127) << 23);
-  if (lane == 0) row_scale[p] = __int_as_float((127 - sigma) << 23);
+  if (lane == 0) rf.write(p, rf.idx[(size_t)perm[p] * k + slot[p]], sigma);
   uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -735,9 +767,11 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
 
 // ---- K-split reduction + SwiGLU, and the combine --------------------------------------
 
-// h16[p][f] = f16( silu(sum_s P[s][p][2f]) * sum_s P[s][p][2f+1] * 2^-8 ) (partials already scaled).
+// h16[p][f] = f16( gn * un * sigmoid(gn * gate_f[p]) * 2^-6 ) with gn, un the normalised
+// gate and up sums over the K splits s ascending.
 __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t slice, int S, int rows, int I,
-                                       uint16_t* __restrict__ h16) {
+                                       const float* __restrict__ gate_f, uint16_t* __restrict__ h16,
+                                       uint32_t* __restrict__ err) {
   pdl_entry();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)rows * I) return;
@@ -748,13 +782,13 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
     g += v.x;
     u += v.y;
   }
-  const float hv = g / (1.f + __expf(-g)) * u * kHScaleInv;
-  h16[i] = __half_as_ushort(__float2half_rn(fminf(fmaxf(hv, -65504.f), 65504.f)));
+  h16[i] = f16_checked(swiglu_store(g, u, g * gate_f[p]), err);
 }
 
-// out[t][c] = bf16_rne( sum over j ascending of w[t][j] * sum over s of Y[s][inv[t*k+j]][c] ),
-// fp32 sums; Y is stored in f16 scaled by 2^-8. Thread per 8 columns; the k rows'
-// loads of a split are issued together.
+// out[t][c] = bf16_rne( sum over j ascending of w[t][j] * comb_f[p] * sum over s of Y[s][p][c] ),
+// p = inv[t*k+j], fp32 sums; Y is stored in f16 in normalised units and comb_f[p] restores
+// the true down projection. Thread per 8 columns; the k rows' loads of a split are issued
+// together.
 __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -766,7 +800,8 @@ __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
 }
 
 __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
-                                  const int32_t* __restrict__ inv, uint16_t* __restrict__ out, int H, int k) {
+                                  const float* __restrict__ comb_f, const int32_t* __restrict__ inv,
+                                  uint16_t* __restrict__ out, int H, int k) {
   pdl_entry();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -779,7 +814,7 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
     for (int j = 0; j < 32; ++j) {
       if (j < k) {
         const int p = inv[(size_t)t * k + j];
-        wj[j] = (p < 0) ? 0.f : w[(size_t)t * k + j] * kYScale;
+        wj[j] = (p < 0) ? 0.f : w[(size_t)t * k + j] * comb_f[p];
         u[j] = (p < 0) ? make_uint4(0, 0, 0, 0) : reinterpret_cast<const uint4*>(y + (size_t)p * H)[c8];
       }
     }
@@ -810,7 +845,7 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (pj[q] < 0) continue;
-        const float wj = w[(size_t)t * k + j0 + q] * kYScale;
+        const float wj = w[(size_t)t * k + j0 + q] * comb_f[pj[q]];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[q][i], acc[i]);
       }
@@ -826,24 +861,107 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
   reinterpret_cast<uint4*>(out + (size_t)t * H)[c8] = packed;
 }
 
-// Inspection: h and y as fp32 (undoing the 2^-8 storage scales), y summed over K splits.
+// Inspection: h and y in true units (fp32), y summed over K splits. Row p's stored h is
+// converted by comb_f[p] / (g_down * 2^n_down) (the combine factor without the down
+// projection's own scale), its stored y by comb_f[p].
 __global__ void debug_hy_kernel(const uint16_t* __restrict__ h16, const uint16_t* __restrict__ ytc, size_t slice,
-                                int S, int rows, int I, int H, float* __restrict__ h, float* __restrict__ y) {
+                                int S, int rows, int I, int H, const float* __restrict__ comb_f,
+                                const int32_t* __restrict__ perm, const int32_t* __restrict__ slot,
+                                const int32_t* __restrict__ idx, int k, const float* __restrict__ dn_global,
+                                const int32_t* __restrict__ norm_exp, float* __restrict__ h, float* __restrict__ y) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (h && i < (size_t)rows * I) h[i] = __half2float(__ushort_as_half(h16[i])) * kHScale;
+  if (h && i < (size_t)rows * I) {
+    const int p = (int)(i / I);
+    const int e = idx[(size_t)perm[p] * k + slot[p]];
+    const float f = ldexpf(comb_f[p] / dn_global[e], -norm_exp[4 * e + 2]);
+    h[i] = __half2float(__ushort_as_half(h16[i])) * f;
+  }
   if (y && i < (size_t)rows * H) {
     float v = 0.f;
     for (int s = 0; s < S; ++s) v += __half2float(__ushort_as_half(ytc[(size_t)s * slice + i]));
-    y[i] = v * kYScale;
+    y[i] = v * comb_f[i / H];
   }
 }
 
-cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, float* h, float* y,
-                            cudaStream_t s) {
+cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
+                            float* h, float* y, cudaStream_t s) {
   const int rows = T * sh.k;
   const size_t n = (size_t)rows * std::max(sh.I, sh.H);
   debug_hy_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.h16, ws.ytc, (size_t)rows * sh.H, pl.S2, rows, sh.I,
-                                                                sh.H, h, y);
+                                                                sh.H, ws.comb_f, ws.perm, ws.slot, ws.idx, sh.k,
+                                                                L.dn_global, L.norm_exp, h, y);
+  return cudaGetLastError();
+}
+
+// ---- load time: accumulator normalisers --------------------------------------------------------
+
+// Largest block scale (as its E4M3 byte; positive bytes order like their values) of the
+// gate rows, the up rows and the down tensor of one expert: maxb[0..2] via atomicMax. The
+// sign bit is ignored and the NaN byte counts as the largest finite one (0x7E).
+__global__ void scale_max_kernel(const uint8_t* __restrict__ gu, size_t n_half, const uint8_t* __restrict__ dn,
+                                 size_t n_dn, uint32_t* __restrict__ maxb) {
+  uint32_t m[3] = {0u, 0u, 0u};
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n_half + n_dn; i += stride) {
+    const int which = i < n_half ? 0 : (i < 2 * n_half ? 1 : 2);
+    uint32_t b = (which < 2 ? gu[i] : dn[i - 2 * n_half]) & 0x7Fu;
+    if (b == 0x7Fu) b = 0x7Eu;
+    m[which] = max(m[which], b);
+  }
+#pragma unroll
+  for (int w = 0; w < 3; ++w) {
+    uint32_t v = m[w];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+    if ((threadIdx.x & 31) == 0 && v) atomicMax(&maxb[w], v);
+  }
+}
+
+cudaError_t launch_scale_max(const Shape& sh, int e, const uint8_t* gu_scales_raw, const uint8_t* dn_scales_raw,
+                             uint32_t* maxb, cudaStream_t s) {
+  const size_t n_half = (size_t)sh.I * (sh.H / 16), n_dn = (size_t)sh.H * (sh.I / 16);
+  scale_max_kernel<<<64, 256, 0, s>>>(gu_scales_raw, n_half, dn_scales_raw, n_dn, maxb + 3 * (size_t)e);
+  return cudaGetLastError();
+}
+
+// Value of a non-negative E4M3 ("fn") byte.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const int ex = (int)((b >> 3) & 15u), mt = (int)(b & 7u);
+  return ex ? ldexpf(1.f + mt / 8.f, ex - 7) : ldexpf((float)mt, -9);
+}
+
+// Smallest n with 2^n >= v (v > 0), exactly.
+__device__ __forceinline__ int ceil_log2(float v) {
+  int ex;
+  const float m = frexpf(v, &ex);  // v = m * 2^ex, m in [0.5, 1)
+  return m == 0.5f ? ex - 1 : ex;
+}
+
+// Per expert: n_gate, n_up = ceil(log2(6 * M)) + 14 and n_down = ceil(log2(6 * M)), M the
+// largest block scale (an all-zero tensor counts as 2^-9, the smallest E4M3 step).
+__global__ void norms_kernel(const uint32_t* __restrict__ maxb, int E, float* __restrict__ gu_norm,
+                             float* __restrict__ dn_norm, int32_t* __restrict__ norm_exp) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  int n[3];
+#pragma unroll
+  for (int w = 0; w < 3; ++w) {
+    const uint32_t b = maxb[3 * e + w];
+    const float M = b ? e4m3_value(b) : ldexpf(1.f, -9);
+    n[w] = ceil_log2(6.f * M) + (w < 2 ? 14 : 0);
+  }
+  gu_norm[2 * e] = ldexpf(1.f, -n[0]);
+  gu_norm[2 * e + 1] = ldexpf(1.f, -n[1]);
+  dn_norm[e] = ldexpf(1.f, -n[2]);
+  norm_exp[4 * e] = n[0];
+  norm_exp[4 * e + 1] = n[1];
+  norm_exp[4 * e + 2] = n[2];
+  norm_exp[4 * e + 3] = 0;
+}
+
+cudaError_t launch_norms(const Shape& sh, const uint32_t* maxb, float* gu_norm, float* dn_norm, int32_t* norm_exp,
+                         cudaStream_t s) {
+  norms_kernel<<<(sh.E + 127) / 128, 128, 0, s>>>(maxb, sh.E, gu_norm, dn_norm, norm_exp);
   return cudaGetLastError();
 }
 
@@ -924,21 +1042,23 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
   return (size_t)std::min<size_t>(sh.E, rows) + rows / pl.nmax + 1;
 }
 
-cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s) {
+cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
+                            cudaStream_t s) {
   cudaError_t e;
   const int n8 = sh.H / 8;
   const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
+  const RowFactors rf{ws.idx, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f};
   if (T < 1024) {  // one warp per routed row
     const int rows = T * sh.k;
     const dim3 grid((rows + 7) / 8), block(256);
-    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
-    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
-    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.xg, ws.row_scale, rows, sh.H);
+    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
+    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
   } else {  // one warp per token, its k rows written from registers
     const dim3 grid((T + 7) / 8), block(256);
-    if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-    else if (maxv == 28) e = launch_pdl(gather_x_f16_kernel<28>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
-    else e = launch_pdl(gather_x_f16_kernel<56>, grid, block, 0, s, x, ws.inv, ws.xg, ws.row_scale, T, sh.H, sh.k);
+    if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_x_f16_kernel<28>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
+    else e = launch_pdl(gather_x_f16_kernel<56>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
   }
   return e;
 }
@@ -983,14 +1103,14 @@ cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const T
   const int rows = T * sh.k;
   const size_t n = (size_t)rows * sh.I;
   return launch_pdl(swiglu_finalize_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ws.part1,
-                    (size_t)rows * 2 * sh.I, pl.S1, rows, sh.I, ws.h16);
+                    (size_t)rows * 2 * sh.I, pl.S1, rows, sh.I, ws.gate_f, ws.h16, ws.err);
 }
 
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
                               cudaStream_t s) {
   dim3 grid((sh.H / 8 + 127) / 128, T);
-  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.inv, out,
-                    sh.H, sh.k);
+  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.comb_f,
+                    ws.inv, out, sh.H, sh.k);
 }
 
 }  // namespace moe

@@ -55,6 +55,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 constexpr uint32_t kErrExpertRange = 1u;
 constexpr uint32_t kErrCountOverflow = 2u;
 // (bit 4 = a bounded wait in the tensor-core GEMM gave up; see tc_ptx.cuh)
+constexpr uint32_t kErrF16Range = 8u;  // a stored f16 intermediate was out of range or not finite
 
 // Profiled stages of one forward.
 enum Stage {
@@ -83,24 +84,40 @@ struct DeviceLayer {
   const uint8_t* dn_tc = nullptr;       // [E][H/128][I/128][9216] down tiles
   const float* gu_global = nullptr;     // [E][2] (gate, up) tensor scales
   const float* dn_global = nullptr;     // [E]
+  const float* gu_norm = nullptr;       // [E][2] 2^-n_gate, 2^-n_up: accumulator normalisers (below)
+  const float* dn_norm = nullptr;       // [E] 2^-n_down
+  const int32_t* norm_exp = nullptr;    // [E][4] (n_gate, n_up, n_down, 0)
 };
 
+// ---- normalised f16 intermediates ----------------------------------------------------------
+// The SwiGLU rows h and the down rows y are stored in f16 between kernels. So that their
+// range does not depend on the size of x or of the tensor scales, they are stored in
+// normalised units. With A = e2m1 * e4m3 (the dequantised weight without its tensor scale,
+// |A| <= 6 * M where M is the projection's largest block scale) and B = the f16 activation
+// row scaled by 2^sigma so its largest element lies in [2^13, 2^14):
+//   gn = acc_gate * 2^-n_gate, un = acc_up * 2^-n_up with 2^n >= 6 * M * 2^14 (so |gn|, |un|
+//        <= H, typically O(1)); exact, being powers of two;
+//   gv = gn * gate_f[p] is the true gate pre-activation (gate_f = g_gate * 2^(n_gate - sigma));
+//   h  = gn * un * sigmoid(gv) * 2^-6 is stored (the true SwiGLU value is h * 2^6 * g_gate *
+//        g_up * 2^(n_gate + n_up - 2 sigma)); x and the tensor scales reach h only through the
+//        bounded sigmoid;
+//   y  = acc_down * 2^-n_down with 2^n_down >= 6 * M_down is stored;
+//   the combine multiplies y by comb_f[p] = g_down * g_gate * g_up * 2^(n_gate + n_up + n_down
+//        + 6 - 2 sigma) (computed in fp32 with ldexp, so it over- or underflows only where the
+//        true output does) and by the gate weight.
+// A stored value that is not finite or beyond the f16 range raises kErrF16Range.
+constexpr float kHStore = 1.0f / 64.0f;
+constexpr int kHStoreExp = 6;
+
 // ---- tensor-core path ------------------------------------------------------------------
-// h is stored in f16 scaled by 2^-8 (overflow only beyond |h| = 1.6e7; below 2^-6
-// the absolute error stays under 2^-17); the down projection's epilogue undoes it.
-constexpr float kHScaleInv = 1.0f / 256.0f;
-constexpr float kHScale = 256.0f;
 constexpr int kTcDecodeN = 16;        // rows per work item, decode variant
 constexpr int kTcDecodeStages = 8;    // shared-memory pipeline stages, decode variant (two CTAs per SM)
 constexpr int kTcDecodeAStages = 3;   // dequantised A stages in TMEM, decode variant
 constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
-constexpr int kTcModePartial = 0;     // epilogue writes scaled fp32 partial sums
-constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes f16 h
-constexpr int kTcModeOutF16 = 2;      // epilogue writes scaled f16 values to out16
-// The down projection's output y is also kept in f16, scaled by 2^-8 (same range
-// and precision argument as h); the combine undoes the scale.
-constexpr float kYScale = 256.0f;
+constexpr int kTcModePartial = 0;     // epilogue writes normalised fp32 partial sums
+constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes normalised f16 h
+constexpr int kTcModeOutF16 = 2;      // epilogue writes normalised f16 values to out16
 
 // A run of at most nmax routed rows of one expert; every (chunk, M tile, K split)
 // is one work item of the grouped GEMM, decoded arithmetically from its index.
@@ -124,10 +141,9 @@ struct TcGemmParams {
   int M = 0, KC = 0, S = 1;
   const TcChunk* chunks = nullptr;
   const int32_t* n_chunks = nullptr;
-  const float* gscale = nullptr;     // tensor scales
+  const float* gscale = nullptr;     // accumulator normalisers 2^-n per expert
   int gstride = 1, gsel = 0;         // gscale[e*gstride + (gsel ? row&1 : 0)]
-  const float* row_scale = nullptr;  // per routed row, or null
-  float post_scale = 1.f;
+  const float* gate_f = nullptr;     // per routed row: normalised gate -> true gate pre-activation
   int mode = kTcModePartial;
   float* out = nullptr;              // partial output [S][rows][ldo]
   uint16_t* out16 = nullptr;         // f16 output [S][rows][ldo] (kTcModeOutF16)
@@ -173,11 +189,12 @@ struct Workspace {
   uint32_t* err = nullptr;        // device error word
   uint32_t* ticket = nullptr;     // CTAs finished in route_small_kernel (zero between calls)
   // tensor-core path
-  uint16_t* xg = nullptr;         // [T*k][H] f16 activation rows in routed order
-  float* row_scale = nullptr;     // [T*k] 2^-sigma of each row of xg
-  uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations (x 2^-8)
-  float* part1 = nullptr;         // [S1][T*k][2I] gate/up partial sums (split K only)
-  uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums (x 2^-8)
+  uint16_t* xg = nullptr;         // [T*k][H] f16 activation rows in routed order (row p x 2^sigma_p)
+  float* gate_f = nullptr;        // [T*k] g_gate * 2^(n_gate - sigma_p) of each routed row
+  float* comb_f = nullptr;        // [T*k] factor from stored y to the true down projection
+  uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations, normalised
+  float* part1 = nullptr;         // [S1][T*k][2I] normalised gate/up partial sums (split K only)
+  uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums, normalised
   TcChunk* chunks = nullptr;     // row chunks of the touched experts (count in meta[2])
   int chunk_cap = 0;
 };
@@ -220,15 +237,22 @@ cudaError_t router_tc_configure();
 
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
-cudaError_t launch_gather_x(const Shape& sh, const Workspace& ws, const uint16_t* x, int T, cudaStream_t s);
+cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
+                            cudaStream_t s);
 // map: activation rows in boxes of 16 rows; map64 / map128: the same tensor in boxes of 64 / 128 rows.
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s);
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
                               cudaStream_t s);
-cudaError_t launch_debug_hy(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, float* h, float* y,
-                            cudaStream_t s);
+cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
+                            float* h, float* y, cudaStream_t s);
+// Load time: largest block scale of each expert's gate, up and down tensors (raw E4M3 bytes in
+// device memory) into maxb[3e..3e+2] (zeroed by the caller), then the normalisers from them.
+cudaError_t launch_scale_max(const Shape& sh, int e, const uint8_t* gu_scales_raw, const uint8_t* dn_scales_raw,
+                             uint32_t* maxb, cudaStream_t s);
+cudaError_t launch_norms(const Shape& sh, const uint32_t* maxb, float* gu_norm, float* dn_norm, int32_t* norm_exp,
+                         cudaStream_t s);
 cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
                              const uint8_t* dn_codes_raw, const uint8_t* dn_scales_raw, uint8_t* gu_tc, uint8_t* dn_tc,
                              cudaStream_t s);

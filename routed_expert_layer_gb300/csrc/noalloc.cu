@@ -12,11 +12,18 @@
 //
 // Set-up: the first call on a device (that device current) looks up the array's
 // device address with cudaGetSymbolAddress and caches it together with the SM
-// count; make that first call before any stream capture. Every call on a device
-// shares the one array and finds the previous call's contents in it; the parts
-// that must start at zero are cleared on the call's stream. Two calls whose work
-// overlaps on the GPU (different streams, no ordering between them) race on the
+// count; make that first call before any stream capture. The address belongs to the
+// device's primary context (the one the CUDA runtime uses); a caller that makes another
+// context current on the same device through the driver API is not supported. Every
+// call on a device shares the one array and finds the previous call's contents in it;
+// the parts that must start at zero are cleared on the call's stream. Two calls whose
+// work overlaps on the GPU (different streams, no ordering between them) race on the
 // array and corrupt each other's results.
+//
+// The logits come from the fp32 SIMT router (one product and one fp32 addition per
+// element of H, in a fixed order), not from the forward path's three-term tensor-core
+// router, so they may differ from moe_forward's in the last bits; two experts whose
+// logits are that close may then be ordered differently.
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -84,9 +91,11 @@ static void setup_device(int dev, DeviceSetup* d) {
 
 extern "C" MOE_API int moe_route_noalloc(void* stream, const void* x, const float* router_w, const float* router_bias,
                                          int32_t H, int32_t E, int32_t k, int32_t T, int32_t* idx, float* w,
-                                         int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
+                                         int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv,
+                                         uint32_t* err) {
   if (!x || !router_w || !idx || !w || !offsets || !perm || !slot || !inv) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (reinterpret_cast<uintptr_t>(err) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
   if (H <= 0 || E <= 0 || k <= 0 || T <= 0) return MOE_ERR_INVALID_ARG;
   if (H % 64 != 0 || k > 32 || k > E) return MOE_ERR_UNSUPPORTED;
   if (T > kMaxTokens || E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
@@ -107,7 +116,7 @@ extern "C" MOE_API int moe_route_noalloc(void* stream, const void* x, const floa
   ws.counts = reinterpret_cast<int32_t*>(base + kOffCounts);
   ws.active = reinterpret_cast<int32_t*>(base + kOffActive);
   ws.meta = reinterpret_cast<int32_t*>(base + kOffMeta);
-  ws.err = base + kOffErr;
+  ws.err = err ? err : base + kOffErr;
   ws.idx = idx;
   ws.w = w;
   ws.offsets = offsets;
@@ -117,8 +126,9 @@ extern "C" MOE_API int moe_route_noalloc(void* stream, const void* x, const floa
   float* zeros = reinterpret_cast<float*>(base + kOffZeros);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the error word accumulates with OR and a missing bias reads zeros: both start at 0
-  if (cudaMemsetAsync(ws.err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the internal error word (used when the caller passes none) accumulates with OR and a
+  // missing bias reads zeros: both start at 0; a caller's error word is the caller's to clear
+  if (!err && cudaMemsetAsync(ws.err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!router_bias && cudaMemsetAsync(zeros, 0, (size_t)E * sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
   DeviceLayer L;
   L.router_w = router_w;

@@ -81,6 +81,7 @@ def check_routing(gpu_logits, gpu_idx, ref_logits, ref_abs, ref_idx, k):
     Returns the boolean mask of near-tie tokens (excluded from output comparisons)."""
     err = np.abs(gpu_logits.astype(np.float64) - ref_logits)
     assert np.all(err <= LOGIT_REL * ref_abs + 1e-30), f"logit error {err.max()} vs bound"
+    print(f"logit error / sum|xW|: max {float(np.max(err / (ref_abs + 1e-300))):.3e} (bound {LOGIT_REL:.3e})")
     delta = 2.0 * float(err.max()) + 1e-12
     ties = near_tie_tokens(ref_logits, k, delta)
     same = np.all(np.sort(gpu_idx, axis=1) == np.sort(ref_idx, axis=1), axis=1)
@@ -92,11 +93,27 @@ def check_routing(gpu_logits, gpu_idx, ref_logits, ref_abs, ref_idx, k):
     return ties
 
 
-def check_output(out_gpu, out_ref, rows_mask=None, tol=TOL_RMS):
+def bf16_half_ulp(v):
+    """Half a unit in the last place of bf16 in the binade of each |v|: the largest error
+    of rounding a real number in that binade to bf16 (8 significant bits)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 8), 2.0 ** -134)
+
+
+def check_output(out_gpu, out_ref, rows_mask=None, tol=TOL_RMS, bf16_out=True):
+    """max |out_gpu - out_ref| <= tol * RMS(out_ref) over the compared rows. For the layer's
+    bf16 output the rounding of each element to bf16 (at most half an ulp of the stored
+    value) is the output format's, not the path's, and is allowed on top: the oracle's own
+    exact result rounded to bf16 would otherwise fail the bound on heavy-tailed rows (on
+    Zipf-routed K3 rows it is 2.8e-2 of RMS off). Returns (max error excess) / RMS."""
     if rows_mask is not None:
         out_gpu, out_ref = out_gpu[rows_mask], out_ref[rows_mask]
     rms = float(np.sqrt(np.mean(out_ref ** 2)))
-    err = float(np.max(np.abs(out_gpu - out_ref))) if out_ref.size else 0.0
     assert np.all(np.isfinite(out_gpu))
+    diff = np.abs(out_gpu - out_ref)
+    if bf16_out:
+        diff = np.maximum(diff - bf16_half_ulp(out_gpu), 0.0)
+    err = float(np.max(diff)) if out_ref.size else 0.0
     assert err <= tol * rms, f"max|err| {err:.4g} > {tol} * RMS {rms:.4g} (ratio {err / rms:.4g})"
     return err / rms if rms > 0 else 0.0

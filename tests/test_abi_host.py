@@ -152,3 +152,37 @@ def test_header_is_plain_c(tmp_path):
         r = subprocess.run([exe, *lang, std, "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(src), "-o",
                             str(tmp_path / f"abi_{cc}.o")], capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_binding_checks_noalloc_arguments():
+    """route_noalloc checks every tensor's dtype, shape and contiguity (and that it is a
+    CUDA tensor) before it hands plain pointers to moe_route_noalloc; each check raises on
+    host tensors here, before any CUDA call."""
+    import torch
+    import routed_expert_layer_gb300 as rel
+    T, H, E, k = 4, 128, 16, 2
+
+    def args(**kw):
+        a = dict(x=torch.zeros(T, H, dtype=torch.int16), router_w=torch.zeros(H, E, dtype=torch.float32),
+                 router_bias=None, k=k, idx=torch.zeros(T, k, dtype=torch.int32),
+                 w=torch.zeros(T, k, dtype=torch.float32), offsets=torch.zeros(E + 1, dtype=torch.int32),
+                 perm=torch.zeros(T * k, dtype=torch.int32), slot=torch.zeros(T * k, dtype=torch.int32),
+                 inv=torch.zeros(T * k, dtype=torch.int32))
+        a.update(kw)
+        return a
+
+    bad = [dict(x=torch.zeros(T, H, dtype=torch.float32)),                  # 4-byte x
+           dict(router_w=torch.zeros(H + 64, E, dtype=torch.float32)),      # H mismatch
+           dict(router_w=torch.zeros(H, E, dtype=torch.float64)),           # router dtype
+           dict(router_bias=torch.zeros(E - 1, dtype=torch.float32)),       # bias size
+           dict(idx=torch.zeros(T, k + 1, dtype=torch.int32)),              # idx shape
+           dict(w=torch.zeros(T, k, dtype=torch.float16)),                  # w dtype
+           dict(offsets=torch.zeros(E, dtype=torch.int32)),                 # offsets size
+           dict(perm=torch.zeros(T * k - 1, dtype=torch.int32)),            # perm size
+           dict(slot=torch.zeros(T * k, dtype=torch.int64)),                # slot dtype
+           dict(inv=torch.zeros(2 * T * k, dtype=torch.int32)[::2]),        # not contiguous
+           dict(err=torch.zeros(2, dtype=torch.int32)),                     # err not one word
+           {}]                                                              # host tensors
+    for kw in bad:
+        with pytest.raises(ValueError):
+            rel.route_noalloc(**args(**kw))

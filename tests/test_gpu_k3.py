@@ -3,10 +3,14 @@
 benchmark times: decode T=1, 8, 53; verify/batched decode T=64, 128, 256;
 prefill T=2048, 4096, 8192; Zipf(1.1)-skewed routing at T=64 and 4096.
 
-Sampled output rows are checked against the oracle token by token (each row
-depends only on its own token); the permutation is checked by properties that
-hold at any size; the selection at full size is checked bit-exactly in
+Sampled output rows (at least 64 per batch, among them every row of the largest
+bucket's first and last row chunk and the last row of a partial chunk) are checked
+against the oracle token by token (each row depends only on its own token); the
+permutation of the whole batch is compared bit for bit with the oracle's permutation
+of the GPU's expert ids; the selection at full size is checked bit-exactly in
 test_gpu_select.py."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -38,40 +42,73 @@ def k3_zipf():
     m.close()
 
 
-def sample_rows(T, n=5, seed=0):
+def rows_per_item(s, T):
+    import torch
+    import routed_expert_layer_gb300 as rel
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    return rel.plan(s["H"], s["I"], s["E"], s["k"], T, sm, T)["rows_per_item"]
+
+
+def sample_rows(r, T, nmax, n=64, per_chunk=24, seed=0):
+    """Every token if T <= n; else the first, middle and last tokens, the tokens of the
+    largest bucket's first and last row chunk (all of them for chunks of at most
+    per_chunk rows, else per_chunk spread over the chunk), the last row of the last
+    expert whose bucket ends in a partial chunk, and random tokens up to n."""
+    if T <= n:
+        return np.arange(T)
+    offs, perm = r["offsets"], r["perm"]
+    counts = np.diff(offs)
+    e = int(np.argmax(counts))
+    c = int(counts[e])
+    first = perm[offs[e]:offs[e] + min(nmax, c)]
+    last = perm[offs[e] + ((c - 1) // nmax) * nmax:offs[e + 1]]
+    rows = {0, T // 2, T - 1}
+    for ch in (first, last):
+        pick = ch if len(ch) <= per_chunk else ch[np.linspace(0, len(ch) - 1, per_chunk).astype(int)]
+        rows |= set(int(v) for v in pick)
+    partial = np.nonzero(counts % nmax != 0)[0]
+    if len(partial):
+        rows.add(int(perm[offs[partial[-1] + 1] - 1]))
     rng = np.random.default_rng(seed + T)
-    rows = {0, T - 1, T // 2} | set(rng.integers(0, T, size=n).tolist())
+    while len(rows) < n:
+        rows.add(int(rng.integers(0, T)))
     return np.array(sorted(rows))
 
 
-def check_permutation_properties(r, T, E, k):
-    offs, perm, slot, inv = r["offsets"], r["perm"], r["slot"], r["inv"]
-    counts = np.diff(offs)
-    assert offs[0] == 0 and offs[-1] == T * k and np.all(counts >= 0)
-    assert np.array_equal(np.bincount(perm, minlength=T), np.full(T, k))
-    assert np.array_equal(inv[perm * k + slot], np.arange(T * k))
-    e_of_row = np.repeat(np.arange(E), counts)
-    assert np.array_equal(r["idx"].reshape(-1)[perm * k + slot], e_of_row)
-    for e in np.nonzero(counts > 1)[0][:200]:  # stable: tokens ascending inside a bucket
-        assert np.all(np.diff(perm[offs[e]:offs[e + 1]]) > 0)
+def check_permutation_exact(r, E):
+    """The GPU's offsets, perm, slot and inv equal the oracle's permutation of the GPU's
+    own expert ids, bit for bit, over the whole batch."""
+    counts, offs, perm, slot, inv = oracle.permute(r["idx"], E)
+    for key, ref in (("offsets", offs), ("perm", perm), ("slot", slot), ("inv", inv)):
+        assert np.array_equal(r[key], ref), key
 
 
-def run_k3(moe, T, zipf=False, name="k3"):
+def scaled_bits(x_bits, a):
+    """bf16 bits of x * 2^a (exact for a power of two away from the format's limits)."""
+    f = synth.bf16_bits_to_f32(x_bits) * np.float32(2.0 ** a)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def run_k3(moe, T, zipf=False, name="k3", L=None, x_scale=0):
     s = SHAPES[name]
-    L = layer(name, zipf)
+    L = layer(name, zipf) if L is None else L
     x = synth.x_bf16(3 + T, T, s["H"])
+    if x_scale:
+        x = scaled_bits(x, x_scale)
     out = gpu_forward(moe, x)
     r = gpu_route(moe, x, s["E"], s["k"])
-    check_permutation_properties(r, T, s["E"], s["k"])
-    rows = sample_rows(T)
+    check_permutation_exact(r, s["E"])
+    rows = sample_rows(r, T, rows_per_item(s, T))
     ref, ref_idx, ref_w, ref_logits = oracle.moe_tokens(oracle.Layer(L), x[rows], s["k"])
     ref_abs = oracle.router_abs(x[rows], L.router_w)
     ties = check_routing(r["logits"][rows], r["idx"][rows], ref_logits, ref_abs, ref_idx, s["k"])
     ratio = check_output(out[rows], ref, ~ties)
+    raw = float(np.max(np.abs(out[rows][~ties] - ref[~ties])) / np.sqrt(np.mean(ref[~ties] ** 2)))
     assert moe.get_error() == 0
     counts = np.diff(r["offsets"])
-    print(f"{name.upper()} T={T} zipf={zipf}: touched={int((counts > 0).sum())} max_rows={int(counts.max())} "
-          f"err/rms={ratio:.3e} near_ties={int(ties.sum())}")
+    print(f"{name.upper()} T={T} zipf={zipf} x_scale={x_scale}: touched={int((counts > 0).sum())} "
+          f"max_rows={int(counts.max())} rows_checked={len(rows)} err/rms={ratio:.3e} (with bf16 output rounding "
+          f"{raw:.3e}) near_ties={int(ties.sum())}")
 
 
 @pytest.mark.parametrize("T", [1, 8, 53, 64, 128, 256, 2048, 4096, 8192])
@@ -82,6 +119,34 @@ def test_k3_uniform(k3, T):
 @pytest.mark.parametrize("T", [64, 4096])
 def test_k3_zipf(k3_zipf, T):
     run_k3(k3_zipf, T, zipf=True)
+
+
+@pytest.mark.parametrize("T", [53, 4096])
+@pytest.mark.parametrize("xa", [-8, 8])
+def test_k3_scaled_x(k3, T, xa):
+    """x scaled by 2^-8 and 2^8 at the decode and prefill sizes."""
+    run_k3(k3, T, x_scale=xa)
+
+
+def k3_scaled_layer():
+    base = layer("k3")
+    return dataclasses.replace(base, gu_global=(base.gu_global * np.float32(64.0)).astype(np.float32),
+                               dn_global=(base.dn_global * np.float32(1 / 64.0)).astype(np.float32))
+
+
+@pytest.fixture(scope="module")
+def k3_scaled():
+    import routed_expert_layer_gb300 as rel
+    m = rel.MoeLayer(K3["H"], K3["I"], K3["E"], K3["k"], 4096)
+    m.load(k3_scaled_layer())
+    yield m
+    m.close()
+
+
+@pytest.mark.parametrize("T", [53, 4096])
+def test_k3_scaled_tensor_scales(k3_scaled, T):
+    """Gate/up tensor scales x 2^6 and down tensor scales x 2^-6."""
+    run_k3(k3_scaled, T, L=k3_scaled_layer())
 
 
 @pytest.fixture(scope="module")

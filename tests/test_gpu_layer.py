@@ -3,6 +3,8 @@ oracle finishes in seconds: the tiny configuration (T=4, H=256, I=128, E=32, k=4
 and a mid shape spanning several tiles with ragged token counts; plus the ABI's
 edge cases (T=0, T=max, bad pointers, forward before load), determinism, the
 host-buffer entry point and the stage hooks."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -37,8 +39,11 @@ def mid():
 
 def run_case(moe, name, T, seed, zipf=False):
     s = SHAPES[name]
-    L = layer(name, zipf)
-    x = synth.x_bf16(seed, T, s["H"])
+    return run_layer_case(moe, layer(name, zipf), s, synth.x_bf16(seed, T, s["H"]))
+
+
+def run_layer_case(moe, L, s, x):
+    """The whole layer on x (bf16 bits) through the C ABI against the oracle on L."""
     ref, ref_idx, ref_w, ref_logits = oracle.moe_forward(oracle.Layer(L), x, s["k"])
     r = gpu_route(moe, x, s["E"], s["k"])
     ref_abs = oracle.router_abs(x, L.router_w)
@@ -78,13 +83,15 @@ def test_mid_zipf_routing():
 H_TOL = 4e-3
 
 
-def test_expert_stage_h_and_y(mid):
-    """h (SwiGLU) and y (down projection) per routed row against the oracle's expert functions."""
+@pytest.mark.parametrize("T", [9, 300])
+def test_expert_stage_h_and_y(mid, T):
+    """h (SwiGLU) and y (down projection) per routed row against the oracle's expert
+    functions, for the decode variant (T=9) and the prefill variant (T=300)."""
     import torch
     s = SHAPES["mid"]
     L = layer("mid")
     OL = oracle.Layer(L)
-    T, k = 9, s["k"]
+    k = s["k"]
     x = synth.x_bf16(55, T, s["H"])
     r = gpu_route(mid, x, s["E"], k)
     h = torch.empty(T * k, s["I"], dtype=torch.float32, device="cuda")
@@ -99,9 +106,9 @@ def test_expert_stage_h_and_y(mid):
         toks = r["perm"][rows]
         href = oracle.expert_gateup(OL, int(e), xf[toks])
         yref = oracle.expert_down(OL, int(e), href)
-        check_output(h[rows], href, tol=H_TOL)
-        check_output(y[rows], oracle.expert_down(OL, int(e), h[rows]), tol=H_TOL)
-        check_output(y[rows], yref, tol=H_TOL)
+        check_output(h[rows], href, tol=H_TOL, bf16_out=False)
+        check_output(y[rows], oracle.expert_down(OL, int(e), h[rows]), tol=H_TOL, bf16_out=False)
+        check_output(y[rows], yref, tol=H_TOL, bf16_out=False)
 
 
 def test_zero_tokens_is_a_noop(tiny):
@@ -225,5 +232,61 @@ def test_degenerate_and_extreme_shapes(name, T):
     m = make(name, 64)
     try:
         run_case(m, name, T, 600 + T)
+    finally:
+        m.close()
+
+
+# ---- the size of x and of the tensor scales ------------------------------------------------
+
+def scaled_bits(x_bits, a):
+    """bf16 bits of x * 2^a (exact for a power of two away from the format's limits)."""
+    f = synth.bf16_bits_to_f32(x_bits) * np.float32(2.0 ** a)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+SCALINGS = [(-8, 0, 0), (8, 0, 0), (0, 6, 0), (0, -6, 0), (0, 0, 6), (0, 0, -6), (8, -6, 6), (-8, 6, -6)]
+
+
+@pytest.mark.parametrize("name,T", [("mid", 9), ("mid", 300), ("wide", 5)])
+@pytest.mark.parametrize("xa,ga,da", SCALINGS)
+def test_scale_of_inputs(name, T, xa, ga, da):
+    """x scaled by 2^xa, the gate/up tensor scales by 2^ga and the down tensor scales by
+    2^da: the layer meets the same tolerance against the oracle at every size of its
+    inputs, for the decode variant (mid T=9), the prefill variant (mid T=300) and the
+    K-split decode path with its separate SwiGLU pass (wide T=5)."""
+    import routed_expert_layer_gb300 as rel
+    s = SHAPES[name]
+    base = layer(name)
+    L = dataclasses.replace(base, gu_global=(base.gu_global * np.float32(2.0 ** ga)).astype(np.float32),
+                            dn_global=(base.dn_global * np.float32(2.0 ** da)).astype(np.float32))
+    x = scaled_bits(synth.x_bf16(900 + T, T, s["H"]), xa)
+    m = rel.MoeLayer(s["H"], s["I"], s["E"], s["k"], T)
+    try:
+        m.load(L)
+        run_layer_case(m, L, s, x)
+    finally:
+        m.close()
+
+
+def test_out_of_range_intermediate_raises_the_error_word():
+    """An input whose SwiGLU values leave the f16 range of the normalised store sets the
+    device error word instead of being clamped silently: every gate/up weight at its
+    largest block value (+6 x 448) and every x element 1.0, so all H = 14336 products of
+    a row add up (normalised gate and up sums of about H/3 each, h about 3e5 > 65504)."""
+    import torch
+    import routed_expert_layer_gb300 as rel
+    s = SHAPES["wide"]
+    base = layer("wide")
+    L = dataclasses.replace(base, gu_codes=np.full_like(base.gu_codes, 0x77),
+                            gu_scales=np.full_like(base.gu_scales, 0x7E))
+    m = rel.MoeLayer(s["H"], s["I"], s["E"], s["k"], 4)
+    try:
+        m.load(L)
+        x = torch.full((4, s["H"]), 0x3F80, dtype=torch.int16, device="cuda")  # bf16 1.0
+        out = torch.empty_like(x)
+        m.forward(x, out)
+        torch.cuda.synchronize()
+        assert m.get_error() & 8
+        assert m.get_error() == 0  # read and cleared
     finally:
         m.close()

@@ -142,13 +142,14 @@ def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2):
     """Device time per forward at one batch size (graph replays over the rotating batches
     xs) with the touched experts, the largest bucket and the roofline fractions."""
     Ts = xs[0].shape[0]
-    msw, _, _ = time_config(moe, xs, reps, warmup, stream)
+    msw, prof, _ = time_config(moe, xs, reps, warmup, stream, profile=True)
     tch = [touched(moe, x, K3["E"], K3["k"]) for x in xs]
     dsw = float(np.mean([t[0] for t in tch]))
     byts = dsw * EXPERT_BYTES
     flops = 6.0 * Ts * K3["k"] * K3["H"] * K3["I"]
     return {"ms": round(msw, 4), "tokens_per_s": round(Ts / (msw * 1e-3), 1), "touched_experts": dsw,
             "largest_bucket": int(max(t[1] for t in tch)), "replays": reps, "batches": len(xs),
+            "stage_ms": {k_: round(v[0] / max(1, v[1]), 4) for k_, v in prof.items() if v[1]},
             "hbm_frac": round(byts / (msw * 1e-3) / 1e9 / hbm, 4),
             "tensor_frac": round(flops / (msw * 1e-3) / 1e12 / bf16, 4)}
 

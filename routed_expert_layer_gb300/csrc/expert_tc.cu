@@ -104,16 +104,22 @@ __device__ __forceinline__ void dequant_unit(const uint4 cw, uint32_t s_lo, uint
 }
 
 // f16 of a normalised intermediate; a value beyond the f16 range or not finite is stored
-// as the conversion gives it (an infinity or NaN, never clamped) and raises the error word.
-__device__ __forceinline__ uint16_t f16_checked(float v, uint32_t* err) {
-  if (!(fabsf(v) <= 65504.f)) atomicOr(err, kErrF16Range);
+// as the conversion gives it (an infinity or NaN, never clamped) and marks `bad`, which the
+// caller turns into one atomicOr of the error word per work item (report_range).
+__device__ __forceinline__ uint16_t f16_checked(float v, bool& bad) {
+  bad |= !(fabsf(v) <= 65504.f);
   return __half_as_ushort(__float2half_rn(v));
 }
 
+__device__ __forceinline__ void report_range(bool bad, uint32_t* err) {
+  if (bad) atomicOr(err, kErrF16Range);
+}
+
 // SwiGLU in normalised units: gn, un normalised gate and up sums, gv the true gate
-// pre-activation; returns gn * un * sigmoid(gv) * 2^-6.
+// pre-activation; returns gn * un * sigmoid(gv) * 2^-6 (fast division: 2 ulp, and a
+// denominator of +inf, from a very negative gv, gives 0).
 __device__ __forceinline__ float swiglu_store(float gn, float un, float gv) {
-  return gn * un * kHStore / (1.f + __expf(-gv));
+  return __fdividef(gn * un * kHStore, 1.f + __expf(-gv));
 }
 
 struct Ring {  // stage index and phase parity of a circular buffer of n slots
@@ -360,6 +366,7 @@ __global__ void __launch_bounds__(kThreadsD, 2)
       if (lane == 0) mbar_arrive(&accempty[b]);
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)];
       const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's normaliser
+      bool bad = false;
 #pragma unroll
       for (int n = 0; n < NMAX; ++n) {
         if (n >= N) break;
@@ -372,16 +379,17 @@ __global__ void __launch_bounds__(kThreadsD, 2)
             const float gn = acc * gsc, un = other * o_gsc;
             const float hv = swiglu_store(gn, un, gn * P.gate_f[p]);
             const int f = m * 64 + (r >> 1);
-            P.h16[(size_t)p * P.I + f] = f16_checked(hv, P.err);
+            P.h16[(size_t)p * P.I + f] = f16_checked(hv, bad);
           }
         } else if (n < ch.n) {
           const size_t o = (size_t)s * P.out_slice + (size_t)p * P.ldo + (size_t)m * 128 + r;
           if (P.mode == kTcModeOutF16)
-            P.out16[o] = f16_checked(acc * gsc, P.err);
+            P.out16[o] = f16_checked(acc * gsc, bad);
           else
             P.out[o] = acc * gsc;
         }
       }
+      report_range(bad, P.err);
     }
   }
   tc_fence_before();
@@ -589,6 +597,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       const int N = ((ch.n + 15) / 16) * 16;
       const float gsc = P.gscale[ch.e * P.gstride + (P.gsel ? (r & 1) : 0)];
       const float o_gsc = __shfl_xor_sync(0xFFFFFFFFu, gsc, 1);  // the partner row's normaliser
+      bool bad = false;
       for (int c0 = hh * (N / 2); c0 < (hh + 1) * (N / 2); c0 += 8) {
         uint32_t v[8];
         float rs8[8];  // gate factors of the 8 rows, loaded ahead of the accumulator read
@@ -609,17 +618,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
               const float gn = acc * gsc, un = other * o_gsc;
               const float hv = swiglu_store(gn, un, gn * rs8[i]);
               const int f = m * 64 + (r >> 1);
-              P.h16[(size_t)p * P.I + f] = f16_checked(hv, P.err);
+              P.h16[(size_t)p * P.I + f] = f16_checked(hv, bad);
             }
           } else if (n < ch.n) {
             const size_t o = (size_t)p * P.ldo + (size_t)m * 128 + r;
             if (P.mode == kTcModeOutF16)
-              P.out16[o] = f16_checked(acc * gsc, P.err);
+              P.out16[o] = f16_checked(acc * gsc, bad);
             else
               P.out[o] = acc * gsc;
           }
         }
       }
+      report_range(bad, P.err);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty);
@@ -782,7 +792,9 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
     g += v.x;
     u += v.y;
   }
-  h16[i] = f16_checked(swiglu_store(g, u, g * gate_f[p]), err);
+  bool bad = false;
+  h16[i] = f16_checked(swiglu_store(g, u, g * gate_f[p]), bad);
+  report_range(bad, err);
 }
 
 // out[t][c] = bf16_rne( sum over j ascending of w[t][j] * comb_f[p] * sum over s of Y[s][p][c] ),

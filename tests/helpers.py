@@ -101,18 +101,28 @@ def bf16_half_ulp(v):
     return np.where(a > 0, 2.0 ** (e - 8), 2.0 ** -134)
 
 
-def check_output(out_gpu, out_ref, rows_mask=None, tol=TOL_RMS, bf16_out=True):
+# The largest relative error of storing a value in f16 (11 significant bits): half an ulp
+# at the bottom of a binade. The SwiGLU and down-projection rows are stored in f16 in
+# normalised units (a factor that is not a power of two away from true units), so in true
+# units only this relative bound holds, not a binade-exact one.
+F16_STORE_REL = 2.0 ** -11
+
+
+def check_output(out_gpu, out_ref, rows_mask=None, tol=TOL_RMS, bf16_out=True, f16_store=False):
     """max |out_gpu - out_ref| <= tol * RMS(out_ref) over the compared rows. For the layer's
     bf16 output the rounding of each element to bf16 (at most half an ulp of the stored
     value) is the output format's, not the path's, and is allowed on top: the oracle's own
     exact result rounded to bf16 would otherwise fail the bound on heavy-tailed rows (on
-    Zipf-routed K3 rows it is 2.8e-2 of RMS off). Returns (max error excess) / RMS."""
+    Zipf-routed K3 rows it is 2.8e-2 of RMS off). f16_store allows instead the rounding of
+    a value stored in f16 (F16_STORE_REL of it). Returns (max error excess) / RMS."""
     if rows_mask is not None:
         out_gpu, out_ref = out_gpu[rows_mask], out_ref[rows_mask]
     rms = float(np.sqrt(np.mean(out_ref ** 2)))
     assert np.all(np.isfinite(out_gpu))
     diff = np.abs(out_gpu - out_ref)
-    if bf16_out:
+    if f16_store:
+        diff = np.maximum(diff - F16_STORE_REL * np.abs(out_gpu), 0.0)
+    elif bf16_out:
         diff = np.maximum(diff - bf16_half_ulp(out_gpu), 0.0)
     err = float(np.max(diff)) if out_ref.size else 0.0
     assert err <= tol * rms, f"max|err| {err:.4g} > {tol} * RMS {rms:.4g} (ratio {err / rms:.4g})"

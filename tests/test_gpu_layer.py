@@ -78,9 +78,14 @@ def test_mid_zipf_routing():
 
 
 # h and y are kept in f16 (11 significant bits) between the GEMMs and before the
-# combine: a relative error of at most 2^-12 per element, i.e. up to about
-# 2^-12 * max|v| / RMS(v) ~ 2e-3 of RMS for Gaussian-like rows.
-H_TOL = 4e-3
+# combine. Each stored element's own rounding (at most 2^-11 of it, helpers.F16_STORE_REL)
+# is allowed per element; what remains is fp32 accumulation and exp() error (about 1e-6
+# relative) for h and for y against the down projection of the GPU's own h, and for y
+# against the oracle's exact h additionally h's rounding carried through W_d (a sum of
+# I independent errors of at most 2^-11 each: about 2^-11 / sqrt(3) of RMS(y) per
+# element, up to ~4 times that at the extremes of a bucket).
+H_TOL = 1e-3
+Y_TOL = 2e-3
 
 
 @pytest.mark.parametrize("T", [9, 300])
@@ -106,9 +111,9 @@ def test_expert_stage_h_and_y(mid, T):
         toks = r["perm"][rows]
         href = oracle.expert_gateup(OL, int(e), xf[toks])
         yref = oracle.expert_down(OL, int(e), href)
-        check_output(h[rows], href, tol=H_TOL, bf16_out=False)
-        check_output(y[rows], oracle.expert_down(OL, int(e), h[rows]), tol=H_TOL, bf16_out=False)
-        check_output(y[rows], yref, tol=H_TOL, bf16_out=False)
+        check_output(h[rows], href, tol=H_TOL, f16_store=True)
+        check_output(y[rows], oracle.expert_down(OL, int(e), h[rows]), tol=H_TOL, f16_store=True)
+        check_output(y[rows], yref, tol=Y_TOL, f16_store=True)
 
 
 def test_zero_tokens_is_a_noop(tiny):

@@ -142,7 +142,10 @@ def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2):
     """Device time per forward at one batch size (graph replays over the rotating batches
     xs) with the touched experts, the largest bucket and the roofline fractions."""
     Ts = xs[0].shape[0]
-    msw, prof, _ = time_config(moe, xs, reps, warmup, stream, profile=True)
+    msw, _, _ = time_config(moe, xs, reps, warmup, stream)
+    # per-stage times from a separate pass: events between the kernels would break the
+    # overlap of programmatic dependent launch in the timed one
+    _, prof, _ = time_config(moe, xs, max(4, reps // 4), 1, stream, profile=True)
     tch = [touched(moe, x, K3["E"], K3["k"]) for x in xs]
     dsw = float(np.mean([t[0] for t in tch]))
     byts = dsw * EXPERT_BYTES

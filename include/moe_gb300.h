@@ -63,26 +63,39 @@ typedef enum {
 /* Layer shape and capacity.
  * Supported: hidden % 256 == 0, inter % 128 == 0, 1 <= top_k <= 32,
  * top_k <= n_experts <= 1024, 1 <= max_tokens, max_tokens * top_k < 2^31,
- * hidden <= 14336. */
+ * hidden <= 14336.
+ * Expert range (expert-parallel serving; "Kimi-K3 NVFP4 station eight sparks", section
+ * "What has to be built": the split is a mask on the router's chosen ids, and the routed
+ * kernel takes a local expert offset): a context may hold only the experts
+ * [expert_begin, expert_begin + expert_count) of the layer's n_experts. The router still
+ * scores all n_experts and every token still picks its top_k among them; routes to
+ * experts outside the range are masked, so the context's output is the part of the
+ * layer's output that its experts contribute, and the outputs of contexts whose ranges
+ * partition the experts add up to the layer. expert_count = 0 (with expert_begin = 0)
+ * means all experts. */
 typedef struct {
-  int32_t hidden;     /* H */
-  int32_t inter;      /* I, the expert intermediate size */
-  int32_t n_experts;  /* E */
-  int32_t top_k;      /* k */
-  int32_t max_tokens; /* the largest T a forward call may pass; sizes the workspace */
-  uint32_t flags;     /* reserved, must be 0 */
+  int32_t hidden;       /* H */
+  int32_t inter;        /* I, the expert intermediate size */
+  int32_t n_experts;    /* E, experts of the layer (the router's outputs) */
+  int32_t top_k;        /* k */
+  int32_t max_tokens;   /* the largest T a forward call may pass; sizes the workspace */
+  uint32_t flags;       /* reserved, must be 0 */
+  int32_t expert_begin; /* first expert this context holds (global id) */
+  int32_t expert_count; /* experts this context holds, or 0 for all n_experts */
 } moe_config;
 
 /* One layer's weights in HOST memory, caller-owned, read only during moe_load_layer.
  * Per-expert pointers let a caller hand over experts wherever they sit (a loader
  * must map expert ids to tensors explicitly; checkpoints may store them out of order).
+ * The expert arrays cover the context's experts only: entry l is global expert
+ * expert_begin + l, for l < n_local (n_local = expert_count, or n_experts for all).
  *   router_w    fp32 [H][E], row-major: logit[t][e] = sum_h x[t][h] * router_w[h][e]
  *   router_bias fp32 [E] added to the logits, or NULL for none
- *   gu_codes[e] uint8 [2I][H/2]: rows 0..I-1 gate, I..2I-1 up; element k of a row is
+ *   gu_codes[l] uint8 [2I][H/2]: rows 0..I-1 gate, I..2I-1 up; element k of a row is
  *               in byte k/2, low nibble = even k; a nibble is an E2M1 code
- *   gu_scales[e] uint8 [2I][H/16]: E4M3 ("fn") scale of elements 16b..16b+15 of a row
- *   gu_global   fp32 [E][2]: (gate, up) tensor scales
- *   dn_codes[e] uint8 [H][I/2], dn_scales[e] uint8 [H][I/16], dn_global fp32 [E]
+ *   gu_scales[l] uint8 [2I][H/16]: E4M3 ("fn") scale of elements 16b..16b+15 of a row
+ *   gu_global   fp32 [n_local][2]: (gate, up) tensor scales
+ *   dn_codes[l] uint8 [H][I/2], dn_scales[l] uint8 [H][I/16], dn_global fp32 [n_local]
  * Weight element = e2m1(code) * e4m3(block scale) * tensor scale. */
 typedef struct {
   const float* router_w;
@@ -116,6 +129,25 @@ MOE_API int moe_load_layer(moe_ctx* ctx, const moe_layer_host* layer);
  * kernels launched without it, copies and events wait for completion as usual. */
 MOE_API int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T);
 
+/* The expert stage on caller-given routing ("Kimi-K3 NVFP4 station eight sparks",
+ * section "What has to be built": a worker takes each token's 16 global expert ids,
+ * with -1 for a masked id, and returns rows plus the ids it actually served):
+ *   out[t][:] = sum over j ascending, where idx[t][j] is one of this context's experts,
+ *               of w[t][j] * FFN_{idx[t][j]}(x[t][:])   (zero if no route is served)
+ *   x       device bf16 [T][H], 16-byte aligned
+ *   idx     device int32 [T][k]: global expert ids; -1 = masked; ids of other contexts'
+ *           experts are skipped. A token must not list one expert twice (error bit 16,
+ *           that token's output is then undefined); an id outside [-1, E) raises error
+ *           bit 1 and is skipped.
+ *   w       device fp32 [T][k]: the weight of each route, applied as given
+ *   out     device bf16 [T][H], 16-byte aligned, must not overlap x
+ *   served  device int32 [T][k] or NULL: idx[t][j] where this context computed the route,
+ *           else -1
+ * Asynchronous on `stream`; allocates nothing; may be captured in a CUDA graph; the same
+ * launch rules as moe_forward. */
+MOE_API int moe_forward_routed(moe_ctx* ctx, void* stream, const void* x, const int32_t* idx, const float* w,
+                               void* out, int32_t T, int32_t* served);
+
 /* The same through HOST buffers: copies x (host bf16 [T][H]) to the device,
  * runs moe_forward, copies the result to out (host bf16 [T][H]) and waits for
  * the stream. Use page-locked host memory for asynchronous copies. */
@@ -133,15 +165,17 @@ MOE_API const char* moe_status_str(int status);
  * 4 = a bounded wait inside a GEMM gave up (the kernel stopped early), 8 = an f16
  * intermediate (SwiGLU or down-projection value, stored in normalised units) was
  * beyond the f16 range or not finite; it is stored as the conversion gives it (an
- * infinity or NaN, never clamped), so the output shows it too. */
+ * infinity or NaN, never clamped), so the output shows it too; 16 = a token of a
+ * caller-given routing listed one expert twice. */
 MOE_API int moe_get_error(moe_ctx* ctx, uint32_t* bits);
 
 /* ---- inspection hooks (tests and benchmarking) ----------------------------- */
 
 /* Routing of T tokens (router, select, permute). Every output is a device
  * pointer and may be NULL:
- *   logits fp32 [T][E]; idx int32 [T][k] (descending logit); w fp32 [T][k];
- *   offsets int32 [E+1]; perm int32 [T*k] (token of routed row p);
+ *   logits fp32 [T][E]; idx int32 [T][k] (descending logit, global ids); w fp32 [T][k];
+ *   offsets int32 [n_local+1] (routed rows of the context's experts; inv = -1 for a
+ *   masked route); perm int32 [T*k] (token of routed row p);
  *   slot int32 [T*k] (j of routed row p); inv int32 [T*k] (row p of (t, j)). */
 MOE_API int moe_debug_route(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* logits, int32_t* idx, float* w,
                     int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv);

@@ -62,6 +62,7 @@ def lib():
         _lib.oracle_expert_down.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p]
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, p, p]
         _lib.oracle_moe_tokens.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, p, p]
+        _lib.oracle_moe_routed.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, i64, p, p]
         _lib.oracle_num_threads.restype = ctypes.c_int
     return _lib
 
@@ -192,6 +193,21 @@ def moe_tokens(L: Layer, x_rows: np.ndarray, k: int):
     if n:
         lib().oracle_moe_tokens(ctypes.byref(L.c), n, k, _ptr(x_rows), _ptr(out), _ptr(idx), _ptr(w), _ptr(logits))
     return out, idx, w, logits
+
+
+def moe_routed(L: Layer, x_bits: np.ndarray, idx: np.ndarray, w: np.ndarray, e0: int = 0):
+    """The expert stage on given routing for a worker holding experts [e0, e0 + L.E) (L
+    holds those experts only): (out fp64 [T][H], served int32 [T][k])."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    T, k = idx.shape
+    out = np.empty((T, L.H), dtype=np.float64)
+    served = np.empty((T, k), dtype=np.int32)
+    if T:
+        lib().oracle_moe_routed(ctypes.byref(L.c), T, k, _ptr(x_bits), _ptr(idx), _ptr(w), e0, _ptr(out),
+                                _ptr(served))
+    return out, served
 
 
 def num_threads() -> int:

@@ -356,6 +356,41 @@ void oracle_moe_tokens(const oracle_layer* L, int64_t n, int64_t k, const uint16
   }
 }
 
+/* The expert stage on given routing for one worker that holds the experts
+ * [e0, e0 + L->E) of a layer ("Kimi-K3 NVFP4 station eight sparks", section "What has
+ * to be built": a worker takes each token's 16 global expert ids, -1 for a masked one,
+ * and returns rows plus the ids it served). L holds the worker's experts only: local
+ * expert l is global expert e0 + l; the router is not used.
+ *   out[t] = sum over j ascending, where e0 <= idx[t][j] < e0 + L->E, of
+ *            w[t][j] * FFN_{idx[t][j]}(x[t])          (zero if no route is served)
+ *   served[t][j] = idx[t][j] for those routes, -1 for every other (may be NULL).
+ * x[T][H] bf16 bits, idx[T][k], w[T][k], out[T][H]. */
+void oracle_moe_routed(const oracle_layer* L, int64_t T, int64_t k, const uint16_t* x, const int32_t* idx,
+                       const double* w, int64_t e0, double* out, int32_t* served) {
+  const int64_t H = L->H, I = L->I, n_local = L->E;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    double* xs = (double*)malloc((size_t)H * sizeof(double));
+    double* hs = (double*)malloc((size_t)I * sizeof(double));
+    double* ys = (double*)malloc((size_t)H * sizeof(double));
+    for (int64_t c = 0; c < H; ++c) xs[c] = oracle_bf16(x[t * H + c]);
+    double* o = out + t * H;
+    for (int64_t c = 0; c < H; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t id = idx[t * k + j];
+      const int mine = id >= e0 && id < e0 + n_local;
+      if (served) served[t * k + j] = mine ? (int32_t)id : -1;
+      if (!mine) continue;
+      oracle_expert_gateup(L, id - e0, 1, xs, hs);
+      oracle_expert_down(L, id - e0, 1, hs, ys);
+      for (int64_t c = 0; c < H; ++c) o[c] += w[t * k + j] * ys[c];
+    }
+    free(xs);
+    free(hs);
+    free(ys);
+  }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

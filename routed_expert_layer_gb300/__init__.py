@@ -31,7 +31,7 @@ MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_DEVICE_FLAG = -4, -5, -6
 EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "moe_destroy", "moe_status_str",
             "moe_get_error", "moe_debug_route", "moe_debug_select", "moe_debug_experts", "moe_profile_stages",
             "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count",
-            "moe_route_noalloc", "moe_plan"]
+            "moe_route_noalloc", "moe_plan", "moe_forward_routed"]
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
@@ -77,7 +77,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
-                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("expert_begin", ctypes.c_int32), ("expert_count", ctypes.c_int32)]
 
 
 class LayerHost(ctypes.Structure):
@@ -103,6 +104,7 @@ def lib():
         L.moe_load_layer.argtypes = [vp, ctypes.POINTER(LayerHost)]
         L.moe_forward.argtypes = [vp, vp, p, p, i32]
         L.moe_forward_host.argtypes = [vp, vp, p, p, i32]
+        L.moe_forward_routed.argtypes = [vp, vp, p, p, p, p, i32, p]
         L.moe_destroy.argtypes = [vp]
         L.moe_status_str.restype = ctypes.c_char_p
         L.moe_status_str.argtypes = [ctypes.c_int]
@@ -220,10 +222,12 @@ def plan(hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, s
 
 
 class MoeLayer:
-    """One routed expert layer on one GPU (wraps a moe_ctx)."""
+    """One routed expert layer on one GPU (wraps a moe_ctx). expert_begin / expert_count
+    select the experts this context holds (0 / 0: all of them)."""
 
-    def __init__(self, hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, device: int = 0):
-        self.cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0)
+    def __init__(self, hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, device: int = 0,
+                 expert_begin: int = 0, expert_count: int = 0):
+        self.cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0, expert_begin, expert_count)
         self.device = device
         self.ctx = ctypes.c_void_p()
         _check(lib().moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self.ctx)), "moe_create")
@@ -236,12 +240,24 @@ class MoeLayer:
     def k(self):
         return self.cfg.top_k
 
+    @property
+    def n_local(self):
+        """Experts this context holds."""
+        return self.cfg.expert_count or self.cfg.n_experts
+
     def load(self, layer) -> None:
-        """layer: object with numpy arrays gu_codes [E][2I][H/2], gu_scales, gu_global [E][2],
-        dn_codes [E][H][I/2], dn_scales, dn_global [E], router_w [H][E], router_bias [E] or None."""
+        """layer: object with numpy arrays gu_codes [n][2I][H/2], gu_scales, gu_global [n][2],
+        dn_codes [n][H][I/2], dn_scales, dn_global [n], router_w [H][E], router_bias [E] or None,
+        where n is either the context's expert count (its experts only) or E (the whole
+        layer, of which the context's range is taken)."""
         E, H, I = self.cfg.n_experts, self.cfg.hidden, self.cfg.inter
-        expect = {"gu_codes": (E, 2 * I, H // 2), "gu_scales": (E, 2 * I, H // 16), "gu_global": (E, 2),
-                  "dn_codes": (E, H, I // 2), "dn_scales": (E, H, I // 16), "dn_global": (E,), "router_w": (H, E)}
+        n, e0 = self.n_local, self.cfg.expert_begin
+        expert_arrays = ("gu_codes", "gu_scales", "gu_global", "dn_codes", "dn_scales", "dn_global")
+        if n != E and len(np.shape(layer.gu_codes)) and np.shape(layer.gu_codes)[0] == E:
+            import dataclasses
+            layer = dataclasses.replace(layer, **{a: getattr(layer, a)[e0:e0 + n] for a in expert_arrays})
+        expect = {"gu_codes": (n, 2 * I, H // 2), "gu_scales": (n, 2 * I, H // 16), "gu_global": (n, 2),
+                  "dn_codes": (n, H, I // 2), "dn_scales": (n, H, I // 16), "dn_global": (n,), "router_w": (H, E)}
         for name, shape in expect.items():  # the library reads these sizes through plain pointers
             if tuple(np.shape(getattr(layer, name))) != shape:
                 raise ValueError(f"{name}: expected shape {list(shape)}, got {list(np.shape(getattr(layer, name)))}")
@@ -256,8 +272,8 @@ class MoeLayer:
 
         def per_expert(a):
             a = arr(a, np.uint8)
-            assert a.shape[0] == E
-            ptrs = (ctypes.c_void_p * E)(*[a.ctypes.data + e * a.strides[0] for e in range(E)])
+            assert a.shape[0] == n
+            ptrs = (ctypes.c_void_p * n)(*[a.ctypes.data + e * a.strides[0] for e in range(n)])
             keep.append(ptrs)
             return ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
 
@@ -276,6 +292,21 @@ class MoeLayer:
         if _rows(out, self.H, "out", True) != T:
             raise ValueError("out: expected as many rows as x")
         _check(lib().moe_forward(self.ctx, _stream(stream), _dptr(x), _dptr(out), T), "moe_forward")
+
+    def forward_routed(self, x, idx, w, out, served=None, stream=None) -> None:
+        """The expert stage on caller-given routing (moe_forward_routed): idx int32 [T][k]
+        global expert ids (-1 masked), w float32 [T][k], served int32 [T][k] or None."""
+        import torch
+        T = _rows(x, self.H, "x", True)
+        if _rows(out, self.H, "out", True) != T:
+            raise ValueError("out: expected as many rows as x")
+        for name, t, dt in (("idx", idx, torch.int32), ("w", w, torch.float32), ("served", served, torch.int32)):
+            if t is None and name == "served":
+                continue
+            if tuple(t.shape) != (T, self.k) or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name}: expected a contiguous CUDA {dt} tensor of shape [{T}][{self.k}]")
+        _check(lib().moe_forward_routed(self.ctx, _stream(stream), _dptr(x), _dptr(idx), _dptr(w), _dptr(out), T,
+                                        _dptr(served)), "moe_forward_routed")
 
     def forward_host(self, x_host, out_host, stream=None) -> None:
         """x_host, out_host: host buffers (numpy uint16 or pinned torch tensors) of [T][H] bf16."""

@@ -102,6 +102,9 @@ int check_config(const moe_config* c) {
   if (c->flags != 0) return MOE_ERR_INVALID_ARG;
   if (c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
+  if (c->expert_begin < 0 || c->expert_count < 0 || (c->expert_count == 0 && c->expert_begin != 0) ||
+      (int64_t)c->expert_begin + c->expert_count > c->n_experts)
+    return MOE_ERR_INVALID_ARG;
   if (c->hidden % 256 != 0 || c->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->hidden > 14336) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED;
@@ -122,10 +125,19 @@ struct Carver {
   }
 };
 
+// The kernels' view of a configuration: the layer's E experts, of which the context
+// holds [e0, e0 + El) (all of them when expert_count is 0).
+Shape shape_of(const moe_config& c) {
+  Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
+  sh.e0 = c.expert_count ? c.expert_begin : 0;
+  sh.El = c.expert_count ? c.expert_count : c.n_experts;
+  return sh;
+}
+
 size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* base) {
-  const size_t T = c.max_tokens, E = c.n_experts, k = c.top_k, H = c.hidden, I = c.inter;
+  const Shape sh = shape_of(c);
+  const size_t T = c.max_tokens, E = c.n_experts, El = sh.El, k = c.top_k, H = c.hidden, I = c.inter;
   const size_t C = (T + 31) / 32;
-  const Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
   // sizes that depend on the per-T plans: the maxima over every T <= max_tokens
   size_t rpart = 1, part1 = 1, ytc = T * k * H, ccap = 1;
   for (int t = 1; t <= c.max_tokens; ++t) {
@@ -142,11 +154,11 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.logits = cv.take<float>(T * E);
   w.idx = cv.take<int32_t>(T * k);
   w.w = cv.take<float>(T * k);
-  w.masks = cv.take<uint32_t>(C * E);
-  w.chunk_base = cv.take<int32_t>(C * E);
-  w.counts = cv.take<int32_t>(E);
-  w.offsets = cv.take<int32_t>(E + 1);
-  w.active = cv.take<int32_t>(E);
+  w.masks = cv.take<uint32_t>(C * El);
+  w.chunk_base = cv.take<int32_t>(C * El);
+  w.counts = cv.take<int32_t>(El);
+  w.offsets = cv.take<int32_t>(El + 1);
+  w.active = cv.take<int32_t>(El);
   w.meta = cv.take<int32_t>(4);
   w.perm = cv.take<int32_t>(T * k);
   w.slot = cv.take<int32_t>(T * k);
@@ -176,20 +188,20 @@ struct WeightPtrs {
 };
 
 size_t weights_layout(const moe_config& c, WeightPtrs* p, char* base) {
-  const size_t E = c.n_experts, H = c.hidden, I = c.inter;
+  const size_t E = c.n_experts, El = shape_of(c).El, H = c.hidden, I = c.inter;
   Carver cv{base};
   WeightPtrs w;
-  w.router_w = cv.take<float>(H * E);
+  w.router_w = cv.take<float>(H * E);  // the router scores all E experts
   w.router_bias = cv.take<float>(E);
-  w.gu_global = cv.take<float>(2 * E);
-  w.dn_global = cv.take<float>(E);
-  w.gu_norm = cv.take<float>(2 * E);
-  w.dn_norm = cv.take<float>(E);
-  w.norm_exp = cv.take<int32_t>(4 * E);
-  w.scale_max = cv.take<uint32_t>(3 * E);
+  w.gu_global = cv.take<float>(2 * El);  // expert tensors: the context's El experts
+  w.dn_global = cv.take<float>(El);
+  w.gu_norm = cv.take<float>(2 * El);
+  w.dn_norm = cv.take<float>(El);
+  w.norm_exp = cv.take<int32_t>(4 * El);
+  w.scale_max = cv.take<uint32_t>(3 * El);
   w.w3 = cv.take<uint16_t>(((E + 127) / 128) * 128 * 3 * H);
-  w.gu_tc = cv.take<uint8_t>(E * 2 * I * H * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
-  w.dn_tc = cv.take<uint8_t>(E * H * I * 9 / 16);
+  w.gu_tc = cv.take<uint8_t>(El * 2 * I * H * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
+  w.dn_tc = cv.take<uint8_t>(El * H * I * 9 / 16);
   if (p) *p = w;
   return cv.off;
 }
@@ -249,14 +261,15 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   return MOE_OK;
 }
 
-// S4..S6 on the tensor cores, for the plan `pl` (the route must have used pl.nmax).
+// S4..S6 on the tensor cores, for the plan `pl` (the route must have used pl.nmax), with
+// the routing idx (global expert ids) and gate weights w.
 int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, const TcPlan& pl,
-                StageTimer* tm) {
+                StageTimer* tm, const int32_t* idx, const float* w) {
   const Shape& sh = ctx->sh;
   const Workspace& ws = ctx->ws;
   const int rows = T * sh.k;
   if (tm) tm->begin(kStagePrep);
-  if (launch_gather_x(sh, ctx->L, ws, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gather_x(sh, ctx->L, ws, idx, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePrep);
 
   TcGemmParams P1;
@@ -309,7 +322,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   if (launch_gemm(pl, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageDown);
   if (tm) tm->begin(kStageCombine);
-  if (launch_combine_tc(sh, ws, pl, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine_tc(sh, ws, pl, w, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageCombine);
   ctx->launches += n;
   return MOE_OK;
@@ -359,7 +372,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   DeviceGuard g(device);
   moe_ctx* ctx = new moe_ctx();
   ctx->cfg = *cfg;
-  ctx->sh = Shape{cfg->hidden, cfg->inter, cfg->n_experts, cfg->top_k};
+  ctx->sh = shape_of(*cfg);
   ctx->device = device;
   ctx->sm_count = prop.multiProcessorCount;
   ctx->ws_bytes = workspace_layout(*cfg, ctx->sm_count, nullptr, nullptr);
@@ -393,8 +406,8 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
       !lh->dn_scales || !lh->dn_global)
     return MOE_ERR_INVALID_ARG;
   const moe_config& c = ctx->cfg;
-  const size_t E = c.n_experts, H = c.hidden, I = c.inter;
-  for (size_t e = 0; e < E; ++e)
+  const size_t E = c.n_experts, El = ctx->sh.El, H = c.hidden, I = c.inter;
+  for (size_t e = 0; e < El; ++e)
     if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   if (!ctx->weights_mem) {
@@ -435,9 +448,9 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
         (lh->router_bias
              ? cudaMemcpy(W.router_bias, lh->router_bias, E * sizeof(float), cudaMemcpyHostToDevice)
              : cudaMemset(W.router_bias, 0, E * sizeof(float))) != cudaSuccess ||
-        cudaMemcpy(W.gu_global, lh->gu_global, 2 * E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(W.dn_global, lh->dn_global, E * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(W.scale_max, 0, 3 * E * sizeof(uint32_t)) != cudaSuccess) {
+        cudaMemcpy(W.gu_global, lh->gu_global, 2 * El * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(W.dn_global, lh->dn_global, El * sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(W.scale_max, 0, 3 * El * sizeof(uint32_t)) != cudaSuccess) {
       st = MOE_ERR_CUDA;
       break;
     }
@@ -446,7 +459,7 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
       st = MOE_ERR_CUDA;
       break;
     }
-    for (size_t e = 0; e < E && st == MOE_OK; ++e) {
+    for (size_t e = 0; e < El && st == MOE_OK; ++e) {
       if (cudaStreamSynchronize(s) != cudaSuccess) {  // the staging buffer is free again
         st = MOE_ERR_CUDA;
         break;
@@ -485,7 +498,25 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   PdlScope pdl(!pl.prefill);
   st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax);
   if (st != MOE_OK) return st;
-  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm);
+  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm, ctx->ws.idx, ctx->ws.w);
+}
+
+int moe_forward_routed(moe_ctx* ctx, void* stream, const void* x, const int32_t* idx, const float* w, void* out,
+                       int32_t T, int32_t* served) {
+  int st = check_forward_args(ctx, x, out, T);
+  if (st != MOE_OK || T == 0) return st;
+  if (!idx || !w || ((uintptr_t)idx & 3u) || ((uintptr_t)w & 3u) || ((uintptr_t)served & 3u))
+    return MOE_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  cudaStream_t s = (cudaStream_t)stream;
+  StageTimer tm(ctx, s);
+  const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
+  PdlScope pdl(!pl.prefill);
+  tm.begin(kStagePermute);
+  if (launch_permute(ctx->sh, ctx->ws, idx, T, s, pl.nmax, served) != cudaSuccess) return MOE_ERR_CUDA;
+  tm.end(kStagePermute);
+  ctx->launches += 3;
+  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm, idx, w);
 }
 
 int moe_forward_host(moe_ctx* ctx, void* stream, const void* x_host, void* out_host, int32_t T) {
@@ -528,13 +559,13 @@ int moe_get_error(moe_ctx* ctx, uint32_t* bits) {
 
 static int copy_route_outputs(moe_ctx* ctx, cudaStream_t s, int T, float* logits, int32_t* idx, float* w,
                               int32_t* offsets, int32_t* perm, int32_t* slot, int32_t* inv) {
-  const size_t E = ctx->cfg.n_experts, k = ctx->cfg.top_k;
+  const size_t E = ctx->cfg.n_experts, El = ctx->sh.El, k = ctx->cfg.top_k;
   struct Item {
     void* dst;
     const void* src;
     size_t bytes;
   } items[] = {{logits, ctx->ws.logits, (size_t)T * E * 4}, {idx, ctx->ws.idx, (size_t)T * k * 4},
-               {w, ctx->ws.w, (size_t)T * k * 4},           {offsets, ctx->ws.offsets, (E + 1) * 4},
+               {w, ctx->ws.w, (size_t)T * k * 4},           {offsets, ctx->ws.offsets, (El + 1) * 4},
                {perm, ctx->ws.perm, (size_t)T * k * 4},     {slot, ctx->ws.slot, (size_t)T * k * 4},
                {inv, ctx->ws.inv, (size_t)T * k * 4}};
   for (const Item& it : items)
@@ -573,7 +604,7 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
   int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, pl.nmax);
   if (st != MOE_OK) return st;
-  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, pl, nullptr);
+  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, pl, nullptr, ctx->ws.idx, ctx->ws.w);
   if (st != MOE_OK) return st;
   return launch_debug_hy(ctx->sh, ctx->L, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -627,7 +658,7 @@ int moe_plan(const moe_config* cfg, int32_t sm_count, int32_t T, int64_t* plan) 
   const int st = check_config(cfg);
   if (st != MOE_OK) return st;
   if (!plan || sm_count < 1 || T < 1 || T > cfg->max_tokens) return MOE_ERR_INVALID_ARG;
-  const Shape sh{cfg->hidden, cfg->inter, cfg->n_experts, cfg->top_k};
+  const Shape sh = shape_of(*cfg);
   const TcPlan pl = tc_plan(sh, T, sm_count);
   const RouterTcPlan rp = router_tc_plan(sh, T, sm_count);
   Workspace w;

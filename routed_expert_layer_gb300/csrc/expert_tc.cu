@@ -653,7 +653,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 // The three tensor scales are split into mantissa and exponent first, so the product
 // over- or underflows only if the result itself does.
 struct RowFactors {
-  const int32_t* idx;
+  const int32_t* idx;  // global expert ids [T][k]; the context's local expert is idx - e0
+  int e0;
   const float* gu_global;
   const float* dn_global;
   const int32_t* norm_exp;
@@ -717,7 +718,7 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
   for (int j = 0; j < k; ++j) {
     const int p = inv[(size_t)t * k + j];
     if (p < 0) continue;
-    if (lane == 0) rf.write(p, rf.idx[(size_t)t * k + j], sigma);
+    if (lane == 0) rf.write(p, rf.idx[(size_t)t * k + j] - rf.e0, sigma);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
@@ -730,14 +731,17 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
 // The same conversion with one warp per routed row p (token perm[p]): every row is
 // produced in parallel, which is what small batches need; large batches use the
 // per-token kernel above, which reads each token row once instead of k times.
+// rows is the launch bound (T * k); *n_rows the routed rows actually present (fewer when
+// routes are masked).
 template <int MAXV>
 __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                        const int32_t* __restrict__ slot, uint16_t* __restrict__ xg,
-                                       const RowFactors rf, int rows, int H, int k) {
+                                       const RowFactors rf, int rows, const int32_t* __restrict__ n_rows, int H,
+                                       int k) {
   pdl_entry();
   const int p = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  if (p >= rows) return;
+  if (p >= rows || p >= *n_rows) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm[p] * H);
   const int n8 = H / 8;
   uint4 v[MAXV];
@@ -759,7 +763,7 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
     sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
   }
   const float sc = __int_as_float((sigma + 127) << 23);
-  if (lane == 0) rf.write(p, rf.idx[(size_t)perm[p] * k + slot[p]], sigma);
+  if (lane == 0) rf.write(p, rf.idx[(size_t)perm[p] * k + slot[p]] - rf.e0, sigma);
   uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -779,13 +783,14 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
 
 // h16[p][f] = f16( gn * un * sigmoid(gn * gate_f[p]) * 2^-6 ) with gn, un the normalised
 // gate and up sums over the K splits s ascending.
-__global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t slice, int S, int rows, int I,
-                                       const float* __restrict__ gate_f, uint16_t* __restrict__ h16,
-                                       uint32_t* __restrict__ err) {
+__global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t slice, int S, int rows,
+                                       const int32_t* __restrict__ n_rows, int I, const float* __restrict__ gate_f,
+                                       uint16_t* __restrict__ h16, uint32_t* __restrict__ err) {
   pdl_entry();
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (size_t)rows * I) return;
   const size_t p = i / I, f = i % I;
+  if (p >= (size_t)*n_rows) return;
   float g = 0.f, u = 0.f;
   for (int s = 0; s < S; ++s) {
     const float2 v = reinterpret_cast<const float2*>(part + (size_t)s * slice + p * 2 * I)[f];
@@ -877,21 +882,30 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
 // converted by comb_f[p] / (g_down * 2^n_down) (the combine factor without the down
 // projection's own scale), its stored y by comb_f[p].
 __global__ void debug_hy_kernel(const uint16_t* __restrict__ h16, const uint16_t* __restrict__ ytc, size_t slice,
-                                int S, int rows, int I, int H, const float* __restrict__ comb_f,
-                                const int32_t* __restrict__ perm, const int32_t* __restrict__ slot,
-                                const int32_t* __restrict__ idx, int k, const float* __restrict__ dn_global,
-                                const int32_t* __restrict__ norm_exp, float* __restrict__ h, float* __restrict__ y) {
+                                int S, int rows, const int32_t* __restrict__ n_rows, int I, int H,
+                                const float* __restrict__ comb_f, const int32_t* __restrict__ perm,
+                                const int32_t* __restrict__ slot, const int32_t* __restrict__ idx, int e0, int k,
+                                const float* __restrict__ dn_global, const int32_t* __restrict__ norm_exp,
+                                float* __restrict__ h, float* __restrict__ y) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t present = (size_t)*n_rows;  // rows beyond it (masked routes) read as zero
   if (h && i < (size_t)rows * I) {
     const int p = (int)(i / I);
-    const int e = idx[(size_t)perm[p] * k + slot[p]];
-    const float f = ldexpf(comb_f[p] / dn_global[e], -norm_exp[4 * e + 2]);
-    h[i] = __half2float(__ushort_as_half(h16[i])) * f;
+    float v = 0.f;
+    if ((size_t)p < present) {
+      const int e = idx[(size_t)perm[p] * k + slot[p]] - e0;
+      const float f = ldexpf(comb_f[p] / dn_global[e], -norm_exp[4 * e + 2]);
+      v = __half2float(__ushort_as_half(h16[i])) * f;
+    }
+    h[i] = v;
   }
   if (y && i < (size_t)rows * H) {
     float v = 0.f;
-    for (int s = 0; s < S; ++s) v += __half2float(__ushort_as_half(ytc[(size_t)s * slice + i]));
-    y[i] = v * comb_f[i / H];
+    if (i / H < present) {
+      for (int s = 0; s < S; ++s) v += __half2float(__ushort_as_half(ytc[(size_t)s * slice + i]));
+      v *= comb_f[i / H];
+    }
+    y[i] = v;
   }
 }
 
@@ -899,9 +913,10 @@ cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspa
                             float* h, float* y, cudaStream_t s) {
   const int rows = T * sh.k;
   const size_t n = (size_t)rows * std::max(sh.I, sh.H);
-  debug_hy_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.h16, ws.ytc, (size_t)rows * sh.H, pl.S2, rows, sh.I,
-                                                                sh.H, ws.comb_f, ws.perm, ws.slot, ws.idx, sh.k,
-                                                                L.dn_global, L.norm_exp, h, y);
+  debug_hy_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.h16, ws.ytc, (size_t)rows * sh.H, pl.S2, rows,
+                                                                ws.offsets + sh.El, sh.I, sh.H, ws.comb_f, ws.perm,
+                                                                ws.slot, ws.idx, sh.e0, sh.k, L.dn_global, L.norm_exp,
+                                                                h, y);
   return cudaGetLastError();
 }
 
@@ -931,7 +946,7 @@ __global__ void scale_max_kernel(const uint8_t* __restrict__ gu, size_t n_half, 
 
 cudaError_t launch_scale_max(const Shape& sh, int e, const uint8_t* gu_scales_raw, const uint8_t* dn_scales_raw,
                              uint32_t* maxb, cudaStream_t s) {
-  const size_t n_half = (size_t)sh.I * (sh.H / 16), n_dn = (size_t)sh.H * (sh.I / 16);
+  const size_t n_half = (size_t)sh.I * (sh.H / 16), n_dn = (size_t)sh.H * (sh.I / 16);  // e is a local expert
   scale_max_kernel<<<64, 256, 0, s>>>(gu_scales_raw, n_half, dn_scales_raw, n_dn, maxb + 3 * (size_t)e);
   return cudaGetLastError();
 }
@@ -973,7 +988,7 @@ __global__ void norms_kernel(const uint32_t* __restrict__ maxb, int E, float* __
 
 cudaError_t launch_norms(const Shape& sh, const uint32_t* maxb, float* gu_norm, float* dn_norm, int32_t* norm_exp,
                          cudaStream_t s) {
-  norms_kernel<<<(sh.E + 127) / 128, 128, 0, s>>>(maxb, sh.E, gu_norm, dn_norm, norm_exp);
+  norms_kernel<<<(sh.El + 127) / 128, 128, 0, s>>>(maxb, sh.El, gu_norm, dn_norm, norm_exp);
   return cudaGetLastError();
 }
 
@@ -1033,8 +1048,8 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   pl.ctas_per_sm = pl.prefill ? 1 : 2;
   pl.grid = sm_count * pl.ctas_per_sm;
   const int M1 = 2 * sh.I / 128, M2 = sh.H / 128, KC1 = sh.H / kChunkK, KC2 = sh.I / kChunkK;
-  // expected touched experts for uniform routing
-  const double d = sh.E * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
+  // expected touched experts of the context for uniform routing
+  const double d = sh.El * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
   const double target = 4.0 * pl.grid;
   auto pick = [&](double items, int KC) {
     int want = (int)ceil(target / (items > 1 ? items : 1));
@@ -1051,21 +1066,22 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
   const TcPlan pl = tc_plan(sh, T, sm_count);
   const size_t rows = (size_t)T * sh.k;
-  return (size_t)std::min<size_t>(sh.E, rows) + rows / pl.nmax + 1;
+  return (size_t)std::min<size_t>(sh.El, rows) + rows / pl.nmax + 1;
 }
 
-cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
-                            cudaStream_t s) {
+cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const int32_t* idx,
+                            const uint16_t* x, int T, cudaStream_t s) {
   cudaError_t e;
   const int n8 = sh.H / 8;
   const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
-  const RowFactors rf{ws.idx, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f};
+  const RowFactors rf{idx, sh.e0, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f};
+  const int32_t* n_rows = ws.offsets + sh.El;
   if (T < 1024) {  // one warp per routed row
     const int rows = T * sh.k;
     const dim3 grid((rows + 7) / 8), block(256);
-    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
-    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
-    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, sh.H, sh.k);
+    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
+    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
   } else {  // one warp per token, its k rows written from registers
     const dim3 grid((T + 7) / 8), block(256);
     if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
@@ -1115,13 +1131,13 @@ cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const T
   const int rows = T * sh.k;
   const size_t n = (size_t)rows * sh.I;
   return launch_pdl(swiglu_finalize_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ws.part1,
-                    (size_t)rows * 2 * sh.I, pl.S1, rows, sh.I, ws.gate_f, ws.h16, ws.err);
+                    (size_t)rows * 2 * sh.I, pl.S1, rows, ws.offsets + sh.El, sh.I, ws.gate_f, ws.h16, ws.err);
 }
 
-cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
-                              cudaStream_t s) {
+cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
+                              int T, cudaStream_t s) {
   dim3 grid((sh.H / 8 + 127) / 128, T);
-  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, ws.w, ws.comb_f,
+  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, w, ws.comb_f,
                     ws.inv, out, sh.H, sh.k);
 }
 

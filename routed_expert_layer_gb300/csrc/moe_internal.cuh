@@ -56,6 +56,7 @@ constexpr uint32_t kErrExpertRange = 1u;
 constexpr uint32_t kErrCountOverflow = 2u;
 // (bit 4 = a bounded wait in the tensor-core GEMM gave up; see tc_ptx.cuh)
 constexpr uint32_t kErrF16Range = 8u;  // a stored f16 intermediate was out of range or not finite
+constexpr uint32_t kErrDuplicate = 16u;  // a token listed the same expert twice (caller-given routing)
 
 // Profiled stages of one forward.
 enum Stage {
@@ -199,9 +200,25 @@ struct Workspace {
   int chunk_cap = 0;
 };
 
+// E is the layer's expert count (the router scores all of them); a context may hold
+// only the experts [e0, e0 + El) (an expert range: expert-parallel serving), and every
+// route to an expert outside it, or with id -1, is masked. Local expert l is global e0 + l.
 struct Shape {
   int H, I, E, k;
+  int e0 = 0, El = 0;
 };
+
+// Global expert id -> local expert of the context, or -1 when the route is masked: id -1,
+// an expert outside the context's range, or (raising kErrExpertRange through `bad`) an id
+// outside [0, E).
+__device__ __forceinline__ int local_expert(int id, int E, int e0, int El, bool& bad) {
+  if (id < -1 || id >= E) {
+    bad = true;
+    return -1;
+  }
+  const int l = id - e0;
+  return (id >= 0 && l >= 0 && l < El) ? l : -1;
+}
 
 // ---- launchers (each enqueues its kernels on `s`) ----------------------------------
 
@@ -223,13 +240,14 @@ cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, fl
 // E % 4 == 0, k <= 32, router K splits <= 64).
 constexpr int kRouteSmallT = 32;
 inline bool route_small_ok(const Shape& sh, int T, int router_splits) {
-  return T <= kRouteSmallT && sh.E <= 1024 && sh.E % 4 == 0 && sh.k <= 32 && router_splits <= 64;
+  return T <= kRouteSmallT && sh.E <= 1024 && sh.E % 4 == 0 && sh.k <= 32 && router_splits <= 64 && sh.El <= 1024;
 }
 cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
                                cudaStream_t s);
-// nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]).
+// nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]);
+// served (may be null) receives idx where the route is served by this context, else -1.
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
-                           int nmax = 0);
+                           int nmax = 0, int32_t* served = nullptr);
 
 // Large-shared-memory opt-in for the kernels that need it (call once per context).
 cudaError_t tc_configure();
@@ -237,14 +255,16 @@ cudaError_t router_tc_configure();
 
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
-cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const uint16_t* x, int T,
-                            cudaStream_t s);
+// idx: the routing whose local routes are gathered (ws.idx, or a caller's).
+cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const int32_t* idx,
+                            const uint16_t* x, int T, cudaStream_t s);
 // map: activation rows in boxes of 16 rows; map64 / map128: the same tensor in boxes of 64 / 128 rows.
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s);
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
-cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int T,
-                              cudaStream_t s);
+// w: the gate weights [T][k] (ws.w, or a caller's).
+cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
+                              int T, cudaStream_t s);
 cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
                             float* h, float* y, cudaStream_t s);
 // Load time: largest block scale of each expert's gate, up and down tensors (raw E4M3 bytes in

@@ -213,31 +213,34 @@ cudaError_t launch_select(const Shape& sh, const float* logits, int32_t* idx, fl
 
 // ---- S3 histogram / prefix sum / permutation --------------------------------------------------
 
-// Per 32-token chunk c and expert e: mask[c][e] bit i set iff token 32c+i chose e.
-// 256 threads = 8 chunks; atomicOr makes the masks independent of thread order.
+// Per 32-token chunk c and local expert l: mask[c][l] bit i set iff token 32c+i chose
+// expert e0 + l (routes with id -1 or outside the context's range are masked). 256
+// threads = 8 chunks; atomicOr makes the masks independent of thread order, and its old
+// value shows a token that listed one expert twice.
 __global__ void __launch_bounds__(256) perm_masks_kernel(const int32_t* __restrict__ idx, uint32_t* __restrict__ masks,
-                                                         uint32_t* __restrict__ err, int T, int E, int k) {
+                                                         uint32_t* __restrict__ err, int T, int E, int e0, int El,
+                                                         int k) {
   pdl_entry();
-  extern __shared__ uint32_t msk[];  // [8][E]
-  for (int i = threadIdx.x; i < 8 * E; i += 256) msk[i] = 0u;
+  extern __shared__ uint32_t msk[];  // [8][El]
+  for (int i = threadIdx.x; i < 8 * El; i += 256) msk[i] = 0u;
   __syncthreads();
   const int cl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 256 + threadIdx.x;
+  bool bad = false, dup = false;
   if (t < T) {
     for (int j = 0; j < k; ++j) {
-      const int e = idx[(size_t)t * k + j];
-      if (e < 0 || e >= E) {
-        atomicOr(err, kErrExpertRange);
-        continue;
-      }
-      atomicOr(&msk[cl * E + e], 1u << lane);
+      const int l = local_expert(idx[(size_t)t * k + j], E, e0, El, bad);
+      if (l < 0) continue;
+      dup |= (atomicOr(&msk[cl * El + l], 1u << lane) >> lane) & 1u;
     }
   }
+  if (bad) atomicOr(err, kErrExpertRange);
+  if (dup) atomicOr(err, kErrDuplicate);
   __syncthreads();
   const int C = (T + 31) / 32;
-  for (int i = threadIdx.x; i < 8 * E; i += 256) {
-    const int c = blockIdx.x * 8 + i / E;
-    if (c < C) masks[(size_t)c * E + (i % E)] = msk[i];
+  for (int i = threadIdx.x; i < 8 * El; i += 256) {
+    const int c = blockIdx.x * 8 + i / El;
+    if (c < C) masks[(size_t)c * El + (i % El)] = msk[i];
   }
 }
 
@@ -270,9 +273,9 @@ __device__ int block_exclusive_scan(int v, int* total) {
   return r;
 }
 
-// One CTA of 1024 threads; thread e walks the chunks in order: chunk_base[c][e] =
-// rows of e in chunks before c; counts, offsets (exclusive scan over e) and the
-// ascending list of touched experts.
+// One CTA of 1024 threads; thread e (a local expert; E here is the context's expert
+// count) walks the chunks in order: chunk_base[c][e] = rows of e in chunks before c;
+// counts, offsets (exclusive scan over e) and the ascending list of touched experts.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restrict__ masks,
                                                          int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ active,
@@ -319,26 +322,31 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restr
   }
 }
 
-// Thread per (t, j): p = offsets[e] + rows of e in earlier chunks + earlier tokens of this chunk.
+// Thread per (t, j): p = offsets[l] + rows of l in earlier chunks + earlier tokens of this
+// chunk, for the route's local expert l; a masked route gets inv = -1 (and served = -1).
 __global__ void perm_scatter_kernel(const int32_t* __restrict__ idx, const uint32_t* __restrict__ masks,
                                     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
                                     int32_t* __restrict__ perm, int32_t* __restrict__ slot, int32_t* __restrict__ inv,
-                                    int T, int E, int k) {
+                                    int32_t* __restrict__ served, int T, int E, int e0, int El, int k) {
   pdl_entry();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * k) return;
   const int t = i / k, j = i % k;
-  const int e = idx[i];
-  if (e < 0 || e >= E) {
+  const int id = idx[i];
+  bool bad = false;  // raised by perm_masks_kernel already
+  const int l = local_expert(id, E, e0, El, bad);
+  if (l < 0) {
     inv[i] = -1;
+    if (served) served[i] = -1;
     return;
   }
   const int c = t >> 5, lane = t & 31;
-  const uint32_t mk = masks[(size_t)c * E + e];
-  const int p = offsets[e] + chunk_base[(size_t)c * E + e] + __popc(mk & ((1u << lane) - 1u));
+  const uint32_t mk = masks[(size_t)c * El + l];
+  const int p = offsets[l] + chunk_base[(size_t)c * El + l] + __popc(mk & ((1u << lane) - 1u));
   perm[p] = t;
   slot[p] = j;
   inv[i] = p;
+  if (served) served[i] = id;
 }
 
 // ---- small batches: S1..S3 after the router GEMM in one CTA -------------------------------
@@ -362,11 +370,11 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
     int32_t* __restrict__ idx, float* __restrict__ w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ active, int32_t* __restrict__ meta, int32_t* __restrict__ perm, int32_t* __restrict__ slot,
     int32_t* __restrict__ inv, TcChunk* __restrict__ chunks, int nmax, int chunk_cap, uint32_t* __restrict__ err,
-    uint32_t* __restrict__ ticket, int T, int E, int k) {
+    uint32_t* __restrict__ ticket, int T, int E, int e0, int El, int k) {
   pdl_entry();
   constexpr int NT = kRouteSmallThreads, G = kRouteSmallGroups;
   __shared__ float4 stage[kRouteSmallMaxS][G];
-  __shared__ uint32_t mask[2 * NT];  // bit t of mask[e]: token t chose expert e
+  __shared__ uint32_t mask[2 * NT];  // bit t of mask[l]: token t chose local expert l
   __shared__ int off_s[2 * NT];
   __shared__ int totals[6];
   __shared__ int max_rows;
@@ -409,38 +417,37 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   for (int t = warp; t < T; t += NT / 32)
     select_token<true>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
   __syncthreads();
+  bool bad = false;
   for (int i = tid; i < T * k; i += NT) {
-    const int e = idx[i];
-    if (e < 0 || e >= E) {
-      atomicOr(err, kErrExpertRange);
-      continue;
-    }
-    atomicOr(&mask[e], 1u << (i / k));
+    const int l = local_expert(idx[i], E, e0, El, bad);
+    if (l >= 0) atomicOr(&mask[l], 1u << (i / k));
   }
+  if (bad) atomicOr(err, kErrExpertRange);
   __syncthreads();
-  const int e0 = tid, e1 = tid + NT;
-  const int run0 = e0 < E ? __popc(mask[e0]) : 0;
-  const int run1 = e1 < E ? __popc(mask[e1]) : 0;
-  if (e0 < E) counts[e0] = run0;
-  if (e1 < E) counts[e1] = run1;
+  // thread tid owns local experts l0 = tid and l1 = tid + NT
+  const int l0 = tid, l1 = tid + NT;
+  const int run0 = l0 < El ? __popc(mask[l0]) : 0;
+  const int run1 = l1 < El ? __popc(mask[l1]) : 0;
+  if (l0 < El) counts[l0] = run0;
+  if (l1 < El) counts[l1] = run1;
   const int rmax = max(run0, run1);
   if (rmax > 0) atomicMax(&max_rows, rmax);
   const int off0 = block_exclusive_scan(run0, &totals[0]);
   const int off1 = block_exclusive_scan(run1, &totals[1]) + totals[0];
   const int pos0 = block_exclusive_scan(run0 > 0 ? 1 : 0, &totals[2]);
   const int pos1 = block_exclusive_scan(run1 > 0 ? 1 : 0, &totals[3]) + totals[2];
-  off_s[e0] = off0;
-  off_s[e1] = off1;
-  if (e0 < E) {
-    offsets[e0] = off0;
-    if (run0 > 0) active[pos0] = e0;
+  off_s[l0] = off0;
+  off_s[l1] = off1;
+  if (l0 < El) {
+    offsets[l0] = off0;
+    if (run0 > 0) active[pos0] = l0;
   }
-  if (e1 < E) {
-    offsets[e1] = off1;
-    if (run1 > 0) active[pos1] = e1;
+  if (l1 < El) {
+    offsets[l1] = off1;
+    if (run1 > 0) active[pos1] = l1;
   }
   if (tid == 0) {
-    offsets[E] = totals[0] + totals[1];
+    offsets[El] = totals[0] + totals[1];
     meta[0] = totals[2] + totals[3];
     meta[1] = max_rows;
   }
@@ -449,9 +456,9 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
     const int cb0 = block_exclusive_scan(nch0, &totals[4]);
     const int cb1 = block_exclusive_scan(nch1, &totals[5]) + totals[4];
     for (int j = 0; j < nch0; ++j)
-      if (cb0 + j < chunk_cap) chunks[cb0 + j] = TcChunk{e0, off0 + j * nmax, min(nmax, run0 - j * nmax), 0};
+      if (cb0 + j < chunk_cap) chunks[cb0 + j] = TcChunk{l0, off0 + j * nmax, min(nmax, run0 - j * nmax), 0};
     for (int j = 0; j < nch1; ++j)
-      if (cb1 + j < chunk_cap) chunks[cb1 + j] = TcChunk{e1, off1 + j * nmax, min(nmax, run1 - j * nmax), 0};
+      if (cb1 + j < chunk_cap) chunks[cb1 + j] = TcChunk{l1, off1 + j * nmax, min(nmax, run1 - j * nmax), 0};
     if (tid == 0) {
       const int tot = totals[4] + totals[5];
       if (tot > chunk_cap) atomicOr(err, kErrCountOverflow);
@@ -461,12 +468,12 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   __syncthreads();
   for (int i = tid; i < T * k; i += NT) {
     const int t = i / k, j = i - t * k;
-    const int ei = idx[i];
-    if (ei < 0 || ei >= E) {
+    const int li = local_expert(idx[i], E, e0, El, bad);
+    if (li < 0) {
       inv[i] = -1;
       continue;
     }
-    const int p = off_s[ei] + __popc(mask[ei] & ((1u << t) - 1u));
+    const int p = off_s[li] + __popc(mask[li] & ((1u << t) - 1u));
     perm[p] = t;
     slot[p] = j;
     inv[i] = p;
@@ -480,22 +487,22 @@ cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Work
   return launch_pdl(route_small_kernel, dim3(grid), dim3(kRouteSmallThreads), 0, s, ws.router_part, L.router_bias, S,
                     ws.logits, ws.idx, ws.w, ws.counts, ws.offsets, ws.active, ws.meta, ws.perm, ws.slot, ws.inv,
                     nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap, ws.err, ws.ticket, T, sh.E,
-                    sh.k);
+                    sh.e0, sh.El, sh.k);
 }
 
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
-                           int nmax) {
+                           int nmax, int32_t* served) {
   const int blocks = (T + 255) / 256;
-  cudaError_t e = launch_pdl(perm_masks_kernel, dim3(blocks), dim3(256), 8 * sh.E * sizeof(uint32_t), s, idx,
-                             ws.masks, ws.err, T, sh.E, sh.k);
+  cudaError_t e = launch_pdl(perm_masks_kernel, dim3(blocks), dim3(256), 8 * sh.El * sizeof(uint32_t), s, idx,
+                             ws.masks, ws.err, T, sh.E, sh.e0, sh.El, sh.k);
   if (e != cudaSuccess) return e;
   e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, ws.masks, ws.chunk_base, ws.counts, ws.offsets,
-                 ws.active, ws.meta, T, sh.E, nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap,
+                 ws.active, ws.meta, T, sh.El, nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap,
                  ws.err);
   if (e != cudaSuccess) return e;
   const int n = T * sh.k;
   return launch_pdl(perm_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, s, idx, ws.masks, ws.chunk_base,
-                    ws.offsets, ws.perm, ws.slot, ws.inv, T, sh.E, sh.k);
+                    ws.offsets, ws.perm, ws.slot, ws.inv, served, T, sh.E, sh.e0, sh.El, sh.k);
 }
 
 }  // namespace moe

@@ -58,6 +58,10 @@ def _cfg(**kw):
     (dict(n_experts=2048), rel.MOE_ERR_UNSUPPORTED),
     (dict(hidden=16384), rel.MOE_ERR_UNSUPPORTED),
     (dict(max_tokens=2**28, top_k=16), rel.MOE_ERR_UNSUPPORTED),
+    (dict(expert_begin=-1, expert_count=4), rel.MOE_ERR_INVALID_ARG),
+    (dict(expert_count=-1), rel.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=5, expert_count=0), rel.MOE_ERR_INVALID_ARG),
+    (dict(expert_begin=30, expert_count=3), rel.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_config_on_host(L, kw, status):
     out = ctypes.c_void_p(1234)
@@ -186,3 +190,18 @@ def test_binding_checks_noalloc_arguments():
     for kw in bad:
         with pytest.raises(ValueError):
             rel.route_noalloc(**args(**kw))
+
+
+def test_plan_of_an_expert_range():
+    """A context holding a quarter of the experts plans for its own experts: fewer row
+    chunks, as many K splits or more (fewer touched experts must still fill the GPU), the
+    same variant choice (rows per expert follow the layer's routing rate, not the range's
+    size)."""
+    full = rel.plan(7168, 1536, 896, 16, 512, 152, 53)
+    cfg = rel.Config(7168, 1536, 896, 16, 512, 0, 224, 224)
+    out = (ctypes.c_int64 * len(rel.PLAN_FIELDS))()
+    assert rel.lib().moe_plan(ctypes.byref(cfg), 152, 53, out) == rel.MOE_OK
+    part = {k: int(v) for k, v in zip(rel.PLAN_FIELDS, out)}
+    assert part["prefill"] == full["prefill"] and part["rows_per_item"] == full["rows_per_item"]
+    assert part["chunk_capacity"] < full["chunk_capacity"]
+    assert part["gateup_splits"] >= full["gateup_splits"] and part["down_splits"] >= full["down_splits"]

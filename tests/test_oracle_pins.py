@@ -300,6 +300,61 @@ def test_zipf_bias_is_a_permuted_log_rank():
     assert len(set(np.argsort(b)[-5:])) == 5
 
 
+# ---- caller-given routing on an expert range (a worker of an expert-parallel split) --------
+
+def _expert_slice(L, e0, n):
+    import dataclasses
+    return dataclasses.replace(L, E=n, **{a: getattr(L, a)[e0:e0 + n] for a in (
+        "gu_codes", "gu_scales", "gu_global", "dn_codes", "dn_scales", "dn_global")})
+
+
+def test_routed_full_range_equals_the_layer():
+    """With the layer's own routing and all experts, the routed expert stage is the layer
+    (same operations in the same order: byte-equal)."""
+    L = synth.layer(H=128, I=64, E=12, seed_weights=61, seed_router=62)
+    x = synth.x_bf16(63, 7, 128)
+    out, idx, w, _ = oracle.moe_forward(oracle.Layer(L), x, 3)
+    got, served = oracle.moe_routed(oracle.Layer(L), x, idx, w, 0)
+    assert np.array_equal(got, out)
+    assert np.array_equal(served, idx)
+
+
+def test_routed_ranges_partition_the_layer():
+    """Workers whose expert ranges partition the experts add up to the layer."""
+    L = synth.layer(H=128, I=64, E=12, seed_weights=61, seed_router=62)
+    x = synth.x_bf16(64, 9, 128)
+    out, idx, w, _ = oracle.moe_forward(oracle.Layer(L), x, 4)
+    parts, served_any = [], np.full(idx.shape, -1)
+    for e0, n in ((0, 5), (5, 1), (6, 6)):
+        got, served = oracle.moe_routed(oracle.Layer(_expert_slice(L, e0, n)), x, idx, w, e0)
+        mine = (idx >= e0) & (idx < e0 + n)
+        assert np.array_equal(served, np.where(mine, idx, -1))
+        served_any = np.where(mine, served, served_any)
+        parts.append(got)
+    assert np.array_equal(served_any, idx)  # every route served exactly once
+    assert np.allclose(sum(parts), out, rtol=1e-12, atol=1e-14)
+
+
+def test_routed_masked_and_foreign_ids_vs_dense_numpy():
+    """Ids -1 and other workers' ids are skipped; the kept routes are weighted as given
+    (dense numpy SwiGLU with the library decoders); no route gives zeros."""
+    L = synth.layer(H=128, I=64, E=10, seed_weights=71, seed_router=72)
+    x = synth.x_bf16(73, 5, 128)
+    idx = np.array([[3, -1, 7, 0], [-1, -1, -1, -1], [9, 4, 5, 2], [6, 3, -1, 8], [1, 2, 3, 4]], dtype=np.int32)
+    w = synth.normal_f32(74, 1, idx.size, 1.0).reshape(idx.shape).astype(np.float64)
+    e0, n = 2, 5  # this worker holds experts 2..6
+    got, served = oracle.moe_routed(oracle.Layer(_expert_slice(L, e0, n)), x, idx, w, e0)
+    xf = bf16_lib(x)
+    ref = np.zeros((5, 128))
+    for t in range(5):
+        for j in range(4):
+            if e0 <= idx[t, j] < e0 + n:
+                ref[t] += w[t, j] * _dense_ffn(L, int(idx[t, j]), xf[t:t + 1])[0]
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-12)
+    assert np.all(got[1] == 0.0)
+    assert np.array_equal(served, np.where((idx >= e0) & (idx < e0 + n), idx, -1))
+
+
 # ---- the pins catch plausible mistakes ------------------------------------------------------
 
 def test_pins_catch_planted_mistakes():

@@ -138,9 +138,18 @@ def make_layer(zipf=False):
     return synth.layer(K3["H"], K3["I"], K3["E"], seed_weights=1, seed_router=2, zipf_seed=4 if zipf else None)
 
 
-def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2):
+# LatentMoE block at the pages' K3 geometry: hidden 7168, routed latent 3584, 896 experts
+# of 3584 x 3072 (18,579,480 B each, the same as the plain K3 layer's), top-16, and the two
+# shared experts (bf16) read as one of intermediate 2 x 3072.
+KB = dict(H=7168, d=3584, I=3072, E=896, k=16, Is=6144)
+KB_DENSE_BYTES = 2 * (2 * KB["d"] * KB["H"]) + 2 * (3 * KB["Is"] * KB["H"])  # bf16 projections + shared
+
+
+def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2, extra_bytes=0, flops_per_token=None):
     """Device time per forward at one batch size (graph replays over the rotating batches
-    xs) with the touched experts, the largest bucket and the roofline fractions."""
+    xs) with the touched experts, the largest bucket and the roofline fractions: bytes =
+    touched experts x 18,579,480 (+ extra_bytes read once per forward), FLOPs = 6 T k H I
+    (or flops_per_token x T)."""
     Ts = xs[0].shape[0]
     msw, _, _ = time_config(moe, xs, reps, warmup, stream)
     # per-stage times from a separate pass: events between the kernels would break the
@@ -148,8 +157,8 @@ def sweep_point(moe, xs, stream, hbm, bf16, reps, warmup=2):
     _, prof, _ = time_config(moe, xs, max(4, reps // 4), 1, stream, profile=True)
     tch = [touched(moe, x, K3["E"], K3["k"]) for x in xs]
     dsw = float(np.mean([t[0] for t in tch]))
-    byts = dsw * EXPERT_BYTES
-    flops = 6.0 * Ts * K3["k"] * K3["H"] * K3["I"]
+    byts = dsw * EXPERT_BYTES + extra_bytes
+    flops = Ts * (flops_per_token if flops_per_token else 6.0 * K3["k"] * K3["H"] * K3["I"])
     return {"ms": round(msw, 4), "tokens_per_s": round(Ts / (msw * 1e-3), 1), "touched_experts": dsw,
             "largest_bucket": int(max(t[1] for t in tch)), "replays": reps, "batches": len(xs),
             "stage_ms": {k_: round(v[0] / max(1, v[1]), 4) for k_, v in prof.items() if v[1]},
@@ -417,6 +426,23 @@ def main():
             sweep[f"zipf_T{Ts}"]["vs_uniform"] = round(sweep[f"T{Ts}"]["ms"] / sweep[f"zipf_T{Ts}"]["ms"], 4)
             del xsw
         mz.close()
+        del zl
+        # the LatentMoE block (routed-down projection and shared experts' gate/up, experts in
+        # the latent, routed-up projection and shared down)
+        bl = synth.block_layer(KB["H"], KB["d"], KB["I"], KB["E"], KB["Is"], seed_weights=1, seed_router=2)
+        mb = rel.MoeLayer(KB["H"], KB["I"], KB["E"], KB["k"], 4096, device=local, latent=KB["d"],
+                          shared_inter=KB["Is"])
+        mb.load(bl)
+        del bl
+        fpt = 6.0 * KB["k"] * KB["d"] * KB["I"] + 2.0 * 2 * KB["d"] * KB["H"] + 6.0 * KB["Is"] * KB["H"]
+        for Ts in (53, 4096):
+            nb = 4 if Ts >= 2048 else 2
+            xsw = [torch.from_numpy(synth.x_bf16(900 + i + Ts, Ts, KB["H"]).view(np.int16)).cuda()
+                   for i in range(nb)]
+            sweep[f"block_T{Ts}"] = sweep_point(mb, xsw, stream, hbm, bf16, reps=30 if Ts <= 256 else 20,
+                                                extra_bytes=KB_DENSE_BYTES, flops_per_token=fpt)
+            del xsw
+        mb.close()
         sweep["clocks"] = sweep_sampler.stop()
 
     cb = None

@@ -72,7 +72,19 @@ typedef enum {
  * experts outside the range are masked, so the context's output is the part of the
  * layer's output that its experts contribute, and the outputs of contexts whose ranges
  * partition the experts add up to the layer. expert_count = 0 (with expert_begin = 0)
- * means all experts. */
+ * means all experts.
+ * LatentMoE block ("Kimi K3 optimization on GB300, Part I", section "Routed-down
+ * projection: column sharding and latent assembly": every MoE block projects the 7,168
+ * hidden dimensions into a 3,584-wide routed latent with a [3584, 7168] BF16 weight, and
+ * back after the experts; "Serving Kimi K3 End to End", section 3.3: 2 shared experts that
+ * every token uses, unquantized in the NVFP4 checkpoint): with latent = d > 0 the routed
+ * experts work in d dimensions,
+ *   lat = bf16(x W_down^T)  (W_down bf16 [d][H]),  routed = the expert sum on lat (width d),
+ *   out = bf16(routed W_up^T + shared(x))  (W_up bf16 [H][d]),
+ * where shared(x) = W_sd (silu(W_sg x) * (W_su x)) with bf16 weights of intermediate size
+ * shared_inter (all shared experts together: two experts of width f are one of width 2f),
+ * present when shared_inter > 0 (only together with latent > 0). The router scores the
+ * hidden state x. Supported: latent % 256 == 0, latent <= 14336, shared_inter % 64 == 0. */
 typedef struct {
   int32_t hidden;       /* H */
   int32_t inter;        /* I, the expert intermediate size */
@@ -82,6 +94,8 @@ typedef struct {
   uint32_t flags;       /* reserved, must be 0 */
   int32_t expert_begin; /* first expert this context holds (global id) */
   int32_t expert_count; /* experts this context holds, or 0 for all n_experts */
+  int32_t latent;       /* d: the routed experts' width in a LatentMoE block, or 0 (they work in H) */
+  int32_t shared_inter; /* intermediate size of the shared experts together, or 0 for none */
 } moe_config;
 
 /* One layer's weights in HOST memory, caller-owned, read only during moe_load_layer.
@@ -96,7 +110,13 @@ typedef struct {
  *   gu_scales[l] uint8 [2I][H/16]: E4M3 ("fn") scale of elements 16b..16b+15 of a row
  *   gu_global   fp32 [n_local][2]: (gate, up) tensor scales
  *   dn_codes[l] uint8 [H][I/2], dn_scales[l] uint8 [H][I/16], dn_global fp32 [n_local]
- * Weight element = e2m1(code) * e4m3(block scale) * tensor scale. */
+ * Weight element = e2m1(code) * e4m3(block scale) * tensor scale. In a LatentMoE block
+ * (latent = d > 0) the expert tensors are at width d in place of H ([2I][d/2], [d][I/2], ...)
+ * and the block's dense weights are bf16 (NULL when not used):
+ *   proj_down   bf16 [d][H]: lat[t][j] = sum_h x[t][h] * proj_down[j][h]
+ *   proj_up     bf16 [H][d]: out[t][c] = sum_j routed[t][j] * proj_up[c][j] + shared
+ *   shared_gu   bf16 [2 Is][H]: rows 0..Is-1 gate, Is..2Is-1 up (Is = shared_inter)
+ *   shared_dn   bf16 [H][Is] */
 typedef struct {
   const float* router_w;
   const float* router_bias;
@@ -106,6 +126,10 @@ typedef struct {
   const uint8_t* const* dn_codes;
   const uint8_t* const* dn_scales;
   const float* dn_global;
+  const uint16_t* proj_down;
+  const uint16_t* proj_up;
+  const uint16_t* shared_gu;
+  const uint16_t* shared_dn;
 } moe_layer_host;
 
 /* Create a context on CUDA device `device`: checks the device is sm_103 and
@@ -187,8 +211,10 @@ MOE_API int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, in
 
 /* The expert stage on its own: runs the whole layer on x and copies the SwiGLU
  * activations h (device fp32 [T*k][I], rows in routed order p) and the
- * unweighted down projections y (device fp32 [T*k][H]) out. Either may be NULL. */
-MOE_API int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y);
+ * unweighted down projections y (device fp32 [T*k][D], D = latent or H) out. Either
+ * may be NULL. In a LatentMoE block, lat (device bf16 [T][d], may be NULL) receives the
+ * routed-down projection the experts read. */
+MOE_API int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y, void* lat);
 
 /* Per-kernel timing with CUDA events recorded on the forward's stream.
  * moe_profile_begin arms the next `max_calls` forwards; moe_profile_end waits

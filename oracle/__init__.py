@@ -42,6 +42,12 @@ class _Layer(ctypes.Structure):
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p)]
 
 
+class _Block(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("d", ctypes.c_int64), ("Is", ctypes.c_int64),
+                ("proj_down", ctypes.c_void_p), ("proj_up", ctypes.c_void_p), ("shared_gu", ctypes.c_void_p),
+                ("shared_dn", ctypes.c_void_p)]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -63,6 +69,7 @@ def lib():
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, p, p]
         _lib.oracle_moe_tokens.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, p, p]
         _lib.oracle_moe_routed.argtypes = [ctypes.POINTER(_Layer), i64, i64, p, p, p, i64, p, p]
+        _lib.oracle_moe_block.argtypes = [ctypes.POINTER(_Layer), ctypes.POINTER(_Block), i64, i64, p, p, p, p, p]
         _lib.oracle_num_threads.restype = ctypes.c_int
     return _lib
 
@@ -208,6 +215,27 @@ def moe_routed(L: Layer, x_bits: np.ndarray, idx: np.ndarray, w: np.ndarray, e0:
         lib().oracle_moe_routed(ctypes.byref(L.c), T, k, _ptr(x_bits), _ptr(idx), _ptr(w), e0, _ptr(out),
                                 _ptr(served))
     return out, served
+
+
+def moe_block(L: Layer, x_rows: np.ndarray, k: int):
+    """A LatentMoE block one token at a time (L from a synth.block_layer: experts at the
+    latent width, the hidden width and the bf16 dense weights): (out [n][hidden], idx,
+    w, logits)."""
+    src = L.src
+    x_rows = np.ascontiguousarray(x_rows, dtype=np.uint16)
+    n = x_rows.shape[0]
+    Is = 0 if src.shared_gu is None else src.shared_gu.shape[0] // 2
+    keep = [np.ascontiguousarray(a, dtype=np.uint16) if a is not None else None
+            for a in (src.proj_down, src.proj_up, src.shared_gu, src.shared_dn)]
+    B = _Block(src.hidden, src.H, Is, *[None if a is None else a.ctypes.data for a in keep])
+    out = np.empty((n, src.hidden), dtype=np.float64)
+    idx = np.empty((n, k), dtype=np.int32)
+    w = np.empty((n, k), dtype=np.float64)
+    logits = np.empty((n, L.E), dtype=np.float64)
+    if n:
+        lib().oracle_moe_block(ctypes.byref(L.c), ctypes.byref(B), n, k, _ptr(x_rows), _ptr(out), _ptr(idx), _ptr(w),
+                               _ptr(logits))
+    return out, idx, w, logits
 
 
 def num_threads() -> int:

@@ -391,6 +391,111 @@ void oracle_moe_routed(const oracle_layer* L, int64_t T, int64_t k, const uint16
   }
 }
 
+/* ---- a LatentMoE block ----------------------------------------------------------- */
+
+/* The dense parts of a LatentMoE block: bf16 bit patterns, row-major. */
+typedef struct {
+  int64_t hidden, d, Is;      /* row width of x and out, routed latent width, shared intermediate */
+  const uint16_t* proj_down;  /* [d][hidden] */
+  const uint16_t* proj_up;    /* [hidden][d] */
+  const uint16_t* shared_gu;  /* [2 Is][hidden]: rows 0..Is-1 gate, Is..2Is-1 up (or NULL) */
+  const uint16_t* shared_dn;  /* [hidden][Is] (or NULL) */
+} oracle_block;
+
+/* One MoE block of a LatentMoE model, one token at a time, in fp64:
+ *   "Kimi K3 optimization on GB300, Part I", section "Routed-down projection": the
+ *   block projects the hidden state into the routed latent with a [d][hidden] bf16
+ *   weight; section "Routed-up projection": back with a weight of the same size after
+ *   the experts; "Serving Kimi K3 End to End", section 3.3: 2 shared experts that every
+ *   token uses (unquantized; all of them here as one SwiGLU of intermediate Is: two
+ *   experts of width f side by side are one of width 2f).
+ *   logits = x W_r (+ bias), x the hidden row; top-k and weights as oracle_select
+ *   lat    = W_down x
+ *   routed = sum over j ascending of w_j FFN_{idx_j}(lat)   (experts of width d = L->H)
+ *   out    = W_up routed + W_sd (silu(W_sg x) * (W_su x))
+ * L holds the experts (width d) and router_w [hidden][E]. */
+void oracle_moe_block(const oracle_layer* L, const oracle_block* B, int64_t n, int64_t k, const uint16_t* x_rows,
+                      double* out, int32_t* idx_out, double* w_out, double* logits_out) {
+  const int64_t Hm = B->hidden, d = B->d, Is = B->Is, I = L->I, E = L->E;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < n; ++t) {
+    double* xs = (double*)malloc((size_t)Hm * sizeof(double));
+    double* logits = (double*)malloc((size_t)E * sizeof(double));
+    double* lat = (double*)malloc((size_t)d * sizeof(double));
+    double* routed = (double*)malloc((size_t)d * sizeof(double));
+    double* hs = (double*)malloc((size_t)(I > Is ? I : Is) * sizeof(double));
+    double* ys = (double*)malloc((size_t)d * sizeof(double));
+    int32_t* idx = (int32_t*)malloc((size_t)k * sizeof(int32_t));
+    double* w = (double*)malloc((size_t)k * sizeof(double));
+    unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+    for (int64_t h = 0; h < Hm; ++h) xs[h] = oracle_bf16(x_rows[t * Hm + h]);
+    /* router on the hidden row, top-k as oracle_select */
+    for (int64_t e = 0; e < E; ++e) logits[e] = 0.0;
+    for (int64_t h = 0; h < Hm; ++h)
+      for (int64_t e = 0; e < E; ++e) logits[e] += xs[h] * (double)L->router_w[h * E + e];
+    if (L->router_bias)
+      for (int64_t e = 0; e < E; ++e) logits[e] += (double)L->router_bias[e];
+    for (int64_t j = 0; j < k; ++j) {
+      int64_t best = -1;
+      for (int64_t e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || logits[e] > logits[best])) best = e;
+      taken[best] = 1;
+      idx[j] = (int32_t)best;
+    }
+    double m = logits[idx[0]], ssum = 0.0;
+    for (int64_t j = 0; j < k; ++j) {
+      w[j] = exp(logits[idx[j]] - m);
+      ssum += w[j];
+    }
+    for (int64_t j = 0; j < k; ++j) w[j] /= ssum;
+    /* routed-down projection */
+    for (int64_t j = 0; j < d; ++j) {
+      double a = 0.0;
+      for (int64_t h = 0; h < Hm; ++h) a += oracle_bf16(B->proj_down[j * Hm + h]) * xs[h];
+      lat[j] = a;
+    }
+    /* routed experts in the latent */
+    for (int64_t c = 0; c < d; ++c) routed[c] = 0.0;
+    for (int64_t j = 0; j < k; ++j) {
+      oracle_expert_gateup(L, idx[j], 1, lat, hs);
+      oracle_expert_down(L, idx[j], 1, hs, ys);
+      for (int64_t c = 0; c < d; ++c) routed[c] += w[j] * ys[c];
+    }
+    /* routed-up projection plus the shared experts */
+    for (int64_t i = 0; i < Is; ++i) {
+      double g = 0.0, u = 0.0;
+      for (int64_t h = 0; h < Hm; ++h) {
+        g += oracle_bf16(B->shared_gu[i * Hm + h]) * xs[h];
+        u += oracle_bf16(B->shared_gu[(Is + i) * Hm + h]) * xs[h];
+      }
+      hs[i] = g / (1.0 + exp(-g)) * u;
+    }
+    double* o = out + t * Hm;
+    for (int64_t c = 0; c < Hm; ++c) {
+      double a = 0.0;
+      for (int64_t j = 0; j < d; ++j) a += oracle_bf16(B->proj_up[c * d + j]) * routed[j];
+      double sh = 0.0;
+      for (int64_t i = 0; i < Is; ++i) sh += oracle_bf16(B->shared_dn[c * Is + i]) * hs[i];
+      o[c] = a + sh;
+    }
+    if (idx_out)
+      for (int64_t j = 0; j < k; ++j) idx_out[t * k + j] = idx[j];
+    if (w_out)
+      for (int64_t j = 0; j < k; ++j) w_out[t * k + j] = w[j];
+    if (logits_out)
+      for (int64_t e = 0; e < E; ++e) logits_out[t * E + e] = logits[e];
+    free(xs);
+    free(logits);
+    free(lat);
+    free(routed);
+    free(hs);
+    free(ys);
+    free(idx);
+    free(w);
+    free(taken);
+  }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

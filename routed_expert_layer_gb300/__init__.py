@@ -19,7 +19,7 @@ _ROOT = os.path.dirname(_HERE)
 _CSRC = os.path.join(_HERE, "csrc")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libmoe_gb300.so")
-_SOURCES = ["api.cu", "route.cu", "router_tc.cu", "expert_tc.cu", "noalloc.cu"]
+_SOURCES = ["api.cu", "route.cu", "router_tc.cu", "expert_tc.cu", "noalloc.cu", "block.cu"]
 _HEADERS = ["moe_internal.cuh", "tc_ptx.cuh"]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -35,8 +35,8 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
-KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-5", "gather": "f16-3",
-              "gateup": "tc-10", "down": "tc-10", "combine": "f32-4"}
+KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-6", "gather": "f16-4",
+              "gateup": "tc-10", "down": "tc-10", "combine": "f32-5"}
 
 
 def _nvcc() -> str:
@@ -78,7 +78,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
 class Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
-                ("expert_begin", ctypes.c_int32), ("expert_count", ctypes.c_int32)]
+                ("expert_begin", ctypes.c_int32), ("expert_count", ctypes.c_int32), ("latent", ctypes.c_int32),
+                ("shared_inter", ctypes.c_int32)]
 
 
 class LayerHost(ctypes.Structure):
@@ -86,7 +87,8 @@ class LayerHost(ctypes.Structure):
                 ("gu_codes", ctypes.POINTER(ctypes.c_void_p)), ("gu_scales", ctypes.POINTER(ctypes.c_void_p)),
                 ("gu_global", ctypes.c_void_p),
                 ("dn_codes", ctypes.POINTER(ctypes.c_void_p)), ("dn_scales", ctypes.POINTER(ctypes.c_void_p)),
-                ("dn_global", ctypes.c_void_p)]
+                ("dn_global", ctypes.c_void_p), ("proj_down", ctypes.c_void_p), ("proj_up", ctypes.c_void_p),
+                ("shared_gu", ctypes.c_void_p), ("shared_dn", ctypes.c_void_p)]
 
 
 _lib = None
@@ -111,7 +113,7 @@ def lib():
         L.moe_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_debug_route.argtypes = [vp, vp, p, i32, p, p, p, p, p, p, p]
         L.moe_debug_select.argtypes = [vp, vp, p, i32, p, p, p, p, p, p]
-        L.moe_debug_experts.argtypes = [vp, vp, p, i32, p, p]
+        L.moe_debug_experts.argtypes = [vp, vp, p, i32, p, p, p]
         L.moe_profile_stage_name.restype = ctypes.c_char_p
         L.moe_profile_stage_name.argtypes = [ctypes.c_int]
         L.moe_profile_begin.argtypes = [vp, i32]
@@ -223,11 +225,14 @@ def plan(hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, s
 
 class MoeLayer:
     """One routed expert layer on one GPU (wraps a moe_ctx). expert_begin / expert_count
-    select the experts this context holds (0 / 0: all of them)."""
+    select the experts this context holds (0 / 0: all of them); latent > 0 makes it a
+    LatentMoE block whose experts work in `latent` dimensions between bf16 routed-down and
+    routed-up projections, with shared experts of total intermediate size shared_inter."""
 
     def __init__(self, hidden: int, inter: int, n_experts: int, top_k: int, max_tokens: int, device: int = 0,
-                 expert_begin: int = 0, expert_count: int = 0):
-        self.cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0, expert_begin, expert_count)
+                 expert_begin: int = 0, expert_count: int = 0, latent: int = 0, shared_inter: int = 0):
+        self.cfg = Config(hidden, inter, n_experts, top_k, max_tokens, 0, expert_begin, expert_count, latent,
+                          shared_inter)
         self.device = device
         self.ctx = ctypes.c_void_p()
         _check(lib().moe_create(ctypes.byref(self.cfg), device, ctypes.byref(self.ctx)), "moe_create")
@@ -241,23 +246,35 @@ class MoeLayer:
         return self.cfg.top_k
 
     @property
+    def D(self):
+        """Width the routed experts work in."""
+        return self.cfg.latent or self.cfg.hidden
+
+    @property
     def n_local(self):
         """Experts this context holds."""
         return self.cfg.expert_count or self.cfg.n_experts
 
     def load(self, layer) -> None:
-        """layer: object with numpy arrays gu_codes [n][2I][H/2], gu_scales, gu_global [n][2],
-        dn_codes [n][H][I/2], dn_scales, dn_global [n], router_w [H][E], router_bias [E] or None,
+        """layer: object with numpy arrays gu_codes [n][2I][D/2], gu_scales, gu_global [n][2],
+        dn_codes [n][D][I/2], dn_scales, dn_global [n], router_w [H][E], router_bias [E] or None,
         where n is either the context's expert count (its experts only) or E (the whole
-        layer, of which the context's range is taken)."""
-        E, H, I = self.cfg.n_experts, self.cfg.hidden, self.cfg.inter
+        layer, of which the context's range is taken) and D the experts' width; for a
+        LatentMoE block also proj_down [d][H], proj_up [H][d], shared_gu [2Is][H] and
+        shared_dn [H][Is] (bf16 bit patterns)."""
+        E, H, I, D = self.cfg.n_experts, self.cfg.hidden, self.cfg.inter, self.D
         n, e0 = self.n_local, self.cfg.expert_begin
         expert_arrays = ("gu_codes", "gu_scales", "gu_global", "dn_codes", "dn_scales", "dn_global")
         if n != E and len(np.shape(layer.gu_codes)) and np.shape(layer.gu_codes)[0] == E:
             import dataclasses
             layer = dataclasses.replace(layer, **{a: getattr(layer, a)[e0:e0 + n] for a in expert_arrays})
-        expect = {"gu_codes": (n, 2 * I, H // 2), "gu_scales": (n, 2 * I, H // 16), "gu_global": (n, 2),
-                  "dn_codes": (n, H, I // 2), "dn_scales": (n, H, I // 16), "dn_global": (n,), "router_w": (H, E)}
+        expect = {"gu_codes": (n, 2 * I, D // 2), "gu_scales": (n, 2 * I, D // 16), "gu_global": (n, 2),
+                  "dn_codes": (n, D, I // 2), "dn_scales": (n, D, I // 16), "dn_global": (n,), "router_w": (H, E)}
+        d, Is = self.cfg.latent, self.cfg.shared_inter
+        if d:
+            expect.update(proj_down=(d, H), proj_up=(H, d))
+        if Is:
+            expect.update(shared_gu=(2 * Is, H), shared_dn=(H, Is))
         for name, shape in expect.items():  # the library reads these sizes through plain pointers
             if tuple(np.shape(getattr(layer, name))) != shape:
                 raise ValueError(f"{name}: expected shape {list(shape)}, got {list(np.shape(getattr(layer, name)))}")
@@ -279,11 +296,17 @@ class MoeLayer:
 
         rw = arr(layer.router_w, np.float32)
         rb = None if layer.router_bias is None else arr(layer.router_bias, np.float32)
+
+        def dense(name):
+            a = getattr(layer, name, None)
+            return None if a is None or name not in expect else arr(a, np.uint16).ctypes.data
+
         lh = LayerHost(rw.ctypes.data, None if rb is None else rb.ctypes.data,
                        per_expert(layer.gu_codes), per_expert(layer.gu_scales),
                        arr(layer.gu_global, np.float32).ctypes.data,
                        per_expert(layer.dn_codes), per_expert(layer.dn_scales),
-                       arr(layer.dn_global, np.float32).ctypes.data)
+                       arr(layer.dn_global, np.float32).ctypes.data,
+                       dense("proj_down"), dense("proj_up"), dense("shared_gu"), dense("shared_dn"))
         _check(lib().moe_load_layer(self.ctx, ctypes.byref(lh)), "moe_load_layer")
 
     def forward(self, x, out, stream=None) -> None:
@@ -294,11 +317,12 @@ class MoeLayer:
         _check(lib().moe_forward(self.ctx, _stream(stream), _dptr(x), _dptr(out), T), "moe_forward")
 
     def forward_routed(self, x, idx, w, out, served=None, stream=None) -> None:
-        """The expert stage on caller-given routing (moe_forward_routed): idx int32 [T][k]
-        global expert ids (-1 masked), w float32 [T][k], served int32 [T][k] or None."""
+        """The expert stage on caller-given routing (moe_forward_routed): x and out [T][D]
+        (the experts' width), idx int32 [T][k] global expert ids (-1 masked), w float32
+        [T][k], served int32 [T][k] or None."""
         import torch
-        T = _rows(x, self.H, "x", True)
-        if _rows(out, self.H, "out", True) != T:
+        T = _rows(x, self.D, "x", True)
+        if _rows(out, self.D, "out", True) != T:
             raise ValueError("out: expected as many rows as x")
         for name, t, dt in (("idx", idx, torch.int32), ("w", w, torch.float32), ("served", served, torch.int32)):
             if t is None and name == "served":
@@ -330,10 +354,10 @@ class MoeLayer:
                                       _dptr(w), _dptr(offsets), _dptr(perm), _dptr(slot), _dptr(inv)),
                "moe_debug_select")
 
-    def debug_experts(self, x, h=None, y=None, stream=None):
+    def debug_experts(self, x, h=None, y=None, lat=None, stream=None):
         _rows(x, self.H, "x", True)
-        _check(lib().moe_debug_experts(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(h), _dptr(y)),
-               "moe_debug_experts")
+        _check(lib().moe_debug_experts(self.ctx, _stream(stream), _dptr(x), x.shape[0], _dptr(h), _dptr(y),
+                                       _dptr(lat)), "moe_debug_experts")
 
     def get_error(self) -> int:
         bits = ctypes.c_uint32(0)

@@ -10,6 +10,10 @@
 //   gate/up GEMM          S4 (+ K-split reduction with SwiGLU when split)
 //   down GEMM             S5
 //   combine               S6
+// In a LatentMoE block (block.cu) the block-in GEMM (routed-down projection and shared
+// experts' gate/up) runs after the routing and the experts read its latent; the combine
+// writes the routed latent next to the shared SwiGLU rows and the block-out GEMM (routed-up
+// projection plus shared down projection, one contraction) writes out.
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -43,6 +47,8 @@ struct moe_ctx {
   CUtensorMap tmap_x128{};
   CUtensorMap tmap_h128{};
   CUtensorMap tmap_w3{};  // bf16 three-term router weights (A of the router GEMM)
+  CUtensorMap tmap_win{};   // LatentMoE block: [W_down ; shared gate/up interleaved] bf16 [d + 2Is][H]
+  CUtensorMap tmap_wout{};  // LatentMoE block: [W_up | shared down] bf16 [H][d + Is]
   // profiling
   int prof_max = 0;
   int prof_calls = 0;
@@ -69,7 +75,8 @@ struct PdlScope {
   ~PdlScope() { g_launch_pdl = false; }
 };
 
-const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep", "gateup", "finalize", "down", "combine"};
+const char* kStageNames[kNumStages] = {"router", "select", "permute", "prep",     "gateup",
+                                       "finalize", "down",  "combine", "block_in", "block_out"};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -107,6 +114,9 @@ int check_config(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->hidden % 256 != 0 || c->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->hidden > 14336) return MOE_ERR_UNSUPPORTED;
+  if (c->latent < 0 || c->shared_inter < 0) return MOE_ERR_INVALID_ARG;
+  if (c->latent % 256 != 0 || c->latent > 14336 || c->shared_inter % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->shared_inter > 0 && c->latent == 0) return MOE_ERR_UNSUPPORTED;  // shared experts ride on the block GEMMs
   if (c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->max_tokens * c->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -131,22 +141,34 @@ Shape shape_of(const moe_config& c) {
   Shape sh{c.hidden, c.inter, c.n_experts, c.top_k};
   sh.e0 = c.expert_count ? c.expert_begin : 0;
   sh.El = c.expert_count ? c.expert_count : c.n_experts;
+  sh.D = c.latent ? c.latent : c.hidden;
   return sh;
 }
 
+bool is_block(const moe_config& c) { return c.latent > 0; }
+
+// The block GEMMs' shapes: block-in M = d + 2 Is over K = H, block-out M = H over K = d + Is.
+int block_in_rows(const moe_config& c) { return c.latent + 2 * c.shared_inter; }
+int block_width(const moe_config& c) { return c.latent + c.shared_inter; }
+
 size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* base) {
   const Shape sh = shape_of(c);
-  const size_t T = c.max_tokens, E = c.n_experts, El = sh.El, k = c.top_k, H = c.hidden, I = c.inter;
+  const size_t T = c.max_tokens, E = c.n_experts, El = sh.El, k = c.top_k, H = c.hidden, I = c.inter, D = sh.D;
   const size_t C = (T + 31) / 32;
   // sizes that depend on the per-T plans: the maxima over every T <= max_tokens
-  size_t rpart = 1, part1 = 1, ytc = T * k * H, ccap = 1;
+  size_t rpart = 1, part1 = 1, ytc = T * k * D, ccap = 1, bpart = 1;
   for (int t = 1; t <= c.max_tokens; ++t) {
     const size_t rows = (size_t)t * k;
     rpart = std::max(rpart, (size_t)router_tc_plan(sh, t, sm_count).S * (size_t)t * E);
     const TcPlan pl = tc_plan(sh, t, sm_count);
     if (pl.S1 > 1) part1 = std::max(part1, (size_t)pl.S1 * rows * 2 * I);
-    ytc = std::max(ytc, (size_t)pl.S2 * rows * H);
+    ytc = std::max(ytc, (size_t)pl.S2 * rows * D);
     ccap = std::max(ccap, tc_chunk_cap(sh, t, sm_count));
+    if (is_block(c)) {
+      const int Mi = block_in_rows(c), Kw = block_width(c);
+      bpart = std::max(bpart, (size_t)dense_tc_plan(Mi, (int)H, t, sm_count).S * (size_t)t * Mi);
+      bpart = std::max(bpart, (size_t)dense_tc_plan((int)H, Kw, t, sm_count).S * (size_t)t * H);
+    }
   }
   Carver cv{base};
   Workspace w;
@@ -167,7 +189,7 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.out_stage = cv.take<uint16_t>(T * H);
   w.err = cv.take<uint32_t>(1);
   w.ticket = cv.take<uint32_t>(1);
-  w.xg = cv.take<uint16_t>(T * k * H);
+  w.xg = cv.take<uint16_t>(T * k * D);
   w.gate_f = cv.take<float>(T * k);
   w.comb_f = cv.take<float>(T * k);
   w.h16 = cv.take<uint16_t>(T * k * I);
@@ -175,6 +197,11 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.ytc = cv.take<uint16_t>(ytc);
   w.chunks = cv.take<TcChunk>(ccap);
   w.chunk_cap = (int)ccap;
+  if (is_block(c)) {
+    w.lat = cv.take<uint16_t>(T * c.latent);
+    w.hcat = cv.take<uint16_t>(T * block_width(c));
+    w.blk_part = cv.take<float>(bpart);
+  }
   if (ws) *ws = w;
   return cv.off;
 }
@@ -185,10 +212,11 @@ struct WeightPtrs {
   uint32_t* scale_max;
   uint16_t* w3;
   uint8_t *gu_tc, *dn_tc;
+  uint16_t *w_in, *w_out;  // LatentMoE block weights (null otherwise)
 };
 
 size_t weights_layout(const moe_config& c, WeightPtrs* p, char* base) {
-  const size_t E = c.n_experts, El = shape_of(c).El, H = c.hidden, I = c.inter;
+  const size_t E = c.n_experts, El = shape_of(c).El, H = c.hidden, I = c.inter, D = shape_of(c).D;
   Carver cv{base};
   WeightPtrs w;
   w.router_w = cv.take<float>(H * E);  // the router scores all E experts
@@ -200,8 +228,10 @@ size_t weights_layout(const moe_config& c, WeightPtrs* p, char* base) {
   w.norm_exp = cv.take<int32_t>(4 * El);
   w.scale_max = cv.take<uint32_t>(3 * El);
   w.w3 = cv.take<uint16_t>(((E + 127) / 128) * 128 * 3 * H);
-  w.gu_tc = cv.take<uint8_t>(El * 2 * I * H * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
-  w.dn_tc = cv.take<uint8_t>(El * H * I * 9 / 16);
+  w.gu_tc = cv.take<uint8_t>(El * 2 * I * D * 9 / 16);  // codes (1/2 B) + scales (1/16 B) per weight
+  w.dn_tc = cv.take<uint8_t>(El * D * I * 9 / 16);
+  w.w_in = is_block(c) ? cv.take<uint16_t>((size_t)block_in_rows(c) * H) : nullptr;
+  w.w_out = is_block(c) ? cv.take<uint16_t>(H * (size_t)block_width(c)) : nullptr;
   if (p) *p = w;
   return cv.off;
 }
@@ -263,7 +293,7 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
 
 // S4..S6 on the tensor cores, for the plan `pl` (the route must have used pl.nmax), with
 // the routing idx (global expert ids) and gate weights w.
-int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int T, const TcPlan& pl,
+int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, int ldo, int T, const TcPlan& pl,
                 StageTimer* tm, const int32_t* idx, const float* w) {
   const Shape& sh = ctx->sh;
   const Workspace& ws = ctx->ws;
@@ -275,7 +305,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   TcGemmParams P1;
   P1.w = ctx->L.gu_tc;
   P1.M = 2 * sh.I / 128;
-  P1.KC = sh.H / 128;
+  P1.KC = sh.D / 128;
   P1.S = pl.S1;
   P1.chunks = ws.chunks;
   P1.n_chunks = ws.meta + 2;
@@ -303,7 +333,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
 
   TcGemmParams P2;
   P2.w = ctx->L.dn_tc;
-  P2.M = sh.H / 128;
+  P2.M = sh.D / 128;
   P2.KC = sh.I / 128;
   P2.S = pl.S2;
   P2.chunks = ws.chunks;
@@ -314,26 +344,59 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P2.gate_f = nullptr;
   P2.mode = kTcModeOutF16;
   P2.out16 = ws.ytc;
-  P2.out_slice = (size_t)rows * sh.H;
-  P2.ldo = sh.H;
+  P2.out_slice = (size_t)rows * sh.D;
+  P2.ldo = sh.D;
   P2.I = sh.I;
   P2.err = ws.err;
   if (tm) tm->begin(kStageDown);
   if (launch_gemm(pl, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageDown);
   if (tm) tm->begin(kStageCombine);
-  if (launch_combine_tc(sh, ws, pl, w, out, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine_tc(sh, ws, pl, w, out, ldo, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageCombine);
   ctx->launches += n;
   return MOE_OK;
 }
 
-int check_forward_args(moe_ctx* ctx, const void* x, const void* out, int32_t T) {
+// LatentMoE block-in: the routed latent (ws.lat) and the shared SwiGLU rows (ws.hcat[:, d:]).
+int run_block_in(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm) {
+  const moe_config& c = ctx->cfg;
+  const int M = block_in_rows(c), d = c.latent, Is = c.shared_inter;
+  const RouterTcPlan pl = dense_tc_plan(M, c.hidden, T, ctx->sm_count);
+  CUtensorMap mx;
+  if (!make_tmap_16(&mx, x, (uint64_t)T, (uint64_t)c.hidden, (uint32_t)pl.nt, true)) return MOE_ERR_CUDA;
+  if (tm) tm->begin(kStageBlockIn);
+  if (launch_dense_tc(pl, ctx->tmap_win, mx, T, M, c.hidden, ctx->ws.blk_part, ctx->ws.err, s) != cudaSuccess ||
+      launch_block_in_finalize(ctx->ws.blk_part, pl.S, T, d, Is, ctx->ws.lat, ctx->ws.hcat, d + Is, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageBlockIn);
+  ctx->launches += 2;
+  return MOE_OK;
+}
+
+// LatentMoE block-out: out = bf16([routed latent | shared SwiGLU] [W_up | W_shared_down]^T).
+int run_block_out(moe_ctx* ctx, cudaStream_t s, uint16_t* out, int T, StageTimer* tm) {
+  const moe_config& c = ctx->cfg;
+  const int K = block_width(c);
+  const RouterTcPlan pl = dense_tc_plan(c.hidden, K, T, ctx->sm_count);
+  CUtensorMap mh;
+  if (!make_tmap_16(&mh, ctx->ws.hcat, (uint64_t)T, (uint64_t)K, (uint32_t)pl.nt, true)) return MOE_ERR_CUDA;
+  if (tm) tm->begin(kStageBlockOut);
+  if (launch_dense_tc(pl, ctx->tmap_wout, mh, T, c.hidden, K, ctx->ws.blk_part, ctx->ws.err, s) != cudaSuccess ||
+      launch_block_out_finalize(ctx->ws.blk_part, pl.S, T, c.hidden, out, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (tm) tm->end(kStageBlockOut);
+  ctx->launches += 2;
+  return MOE_OK;
+}
+
+// width: the row width of x and out (H for the layer, D for the expert stage alone).
+int check_forward_args(moe_ctx* ctx, const void* x, const void* out, int32_t T, int width) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > ctx->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  const size_t bytes = (size_t)T * ctx->cfg.hidden * 2;
+  const size_t bytes = (size_t)T * width * 2;
   const char* xa = (const char*)x;
   const char* oa = (const char*)out;
   if (xa < oa + bytes && oa < xa + bytes) return MOE_ERR_INVALID_ARG;
@@ -385,11 +448,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const uint64_t rows = (uint64_t)cfg->max_tokens * cfg->top_k;
   if (cudaMemset(ctx->ws.err, 0, sizeof(uint32_t)) != cudaSuccess ||
       cudaMemset(ctx->ws.ticket, 0, sizeof(uint32_t)) != cudaSuccess ||
-      !make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, cfg->hidden, 16, false) ||
+      !make_tmap_16(&ctx->tmap_x, ctx->ws.xg, rows, ctx->sh.D, 16, false) ||
       !make_tmap_16(&ctx->tmap_h, ctx->ws.h16, rows, cfg->inter, 16, false) ||
-      !make_tmap_16(&ctx->tmap_x64, ctx->ws.xg, rows, cfg->hidden, 64, false) ||
+      !make_tmap_16(&ctx->tmap_x64, ctx->ws.xg, rows, ctx->sh.D, 64, false) ||
       !make_tmap_16(&ctx->tmap_h64, ctx->ws.h16, rows, cfg->inter, 64, false) ||
-      !make_tmap_16(&ctx->tmap_x128, ctx->ws.xg, rows, cfg->hidden, 128, false) ||
+      !make_tmap_16(&ctx->tmap_x128, ctx->ws.xg, rows, ctx->sh.D, 128, false) ||
       !make_tmap_16(&ctx->tmap_h128, ctx->ws.h16, rows, cfg->inter, 128, false) || tc_configure() != cudaSuccess ||
       router_tc_configure() != cudaSuccess) {
     cudaGetLastError();
@@ -406,9 +469,11 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
       !lh->dn_scales || !lh->dn_global)
     return MOE_ERR_INVALID_ARG;
   const moe_config& c = ctx->cfg;
-  const size_t E = c.n_experts, El = ctx->sh.El, H = c.hidden, I = c.inter;
+  const size_t E = c.n_experts, El = ctx->sh.El, H = c.hidden, I = c.inter, D = ctx->sh.D;
   for (size_t e = 0; e < El; ++e)
     if (!lh->gu_codes[e] || !lh->gu_scales[e] || !lh->dn_codes[e] || !lh->dn_scales[e]) return MOE_ERR_INVALID_ARG;
+  if (is_block(c) && (!lh->proj_down || !lh->proj_up)) return MOE_ERR_INVALID_ARG;
+  if (c.shared_inter > 0 && (!lh->shared_gu || !lh->shared_dn)) return MOE_ERR_INVALID_ARG;
   DeviceGuard g(ctx->device);
   if (!ctx->weights_mem) {
     ctx->weights_bytes = weights_layout(c, nullptr, nullptr);
@@ -431,7 +496,7 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
   ctx->L.norm_exp = W.norm_exp;
   ctx->L.gu_tc = W.gu_tc;
   ctx->L.dn_tc = W.dn_tc;
-  const size_t gu_cb = 2 * I * (H / 2), gu_sb = 2 * I * (H / 16), dn_cb = H * (I / 2), dn_sb = H * (I / 16);
+  const size_t gu_cb = 2 * I * (D / 2), gu_sb = 2 * I * (D / 16), dn_cb = D * (I / 2), dn_sb = D * (I / 16);
   uint8_t* staging = nullptr;
   if (cudaMalloc(&staging, gu_cb + gu_sb + dn_cb + dn_sb) != cudaSuccess) {
     cudaGetLastError();
@@ -458,6 +523,25 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
         !make_tmap_16(&ctx->tmap_w3, W.w3, ((E + 127) / 128) * 128, 3 * H, 128, true)) {
       st = MOE_ERR_CUDA;
       break;
+    }
+    if (is_block(c)) {
+      // block-in weights: W_down rows, then the shared gate and up rows interleaved (row
+      // d + 2i gate i, d + 2i + 1 up i) so a SwiGLU pair sits in adjacent accumulator lanes;
+      // block-out weights: each row c is W_up[c][:] followed by W_shared_down[c][:]
+      const size_t d = c.latent, Is = c.shared_inter, Kw = block_width(c), rb = H * 2;
+      if (cudaMemcpy(W.w_in, lh->proj_down, d * rb, cudaMemcpyHostToDevice) != cudaSuccess ||
+          (Is && (cudaMemcpy2D(W.w_in + d * H, 2 * rb, lh->shared_gu, rb, rb, Is, cudaMemcpyHostToDevice) !=
+                      cudaSuccess ||
+                  cudaMemcpy2D(W.w_in + (d + 1) * H, 2 * rb, lh->shared_gu + Is * H, rb, rb, Is,
+                               cudaMemcpyHostToDevice) != cudaSuccess)) ||
+          cudaMemcpy2D(W.w_out, Kw * 2, lh->proj_up, d * 2, d * 2, H, cudaMemcpyHostToDevice) != cudaSuccess ||
+          (Is && cudaMemcpy2D(W.w_out + d, Kw * 2, lh->shared_dn, Is * 2, Is * 2, H, cudaMemcpyHostToDevice) !=
+                     cudaSuccess) ||
+          !make_tmap_16(&ctx->tmap_win, W.w_in, (uint64_t)block_in_rows(c), H, 128, true) ||
+          !make_tmap_16(&ctx->tmap_wout, W.w_out, H, Kw, 128, true)) {
+        st = MOE_ERR_CUDA;
+        break;
+      }
     }
     for (size_t e = 0; e < El && st == MOE_OK; ++e) {
       if (cudaStreamSynchronize(s) != cudaSuccess) {  // the staging buffer is free again
@@ -489,7 +573,7 @@ int moe_load_layer(moe_ctx* ctx, const moe_layer_host* lh) {
 }
 
 int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T) {
-  int st = check_forward_args(ctx, x, out, T);
+  int st = check_forward_args(ctx, x, out, T, ctx ? ctx->cfg.hidden : 0);
   if (st != MOE_OK || T == 0) return st;
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
@@ -498,12 +582,19 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   PdlScope pdl(!pl.prefill);
   st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax);
   if (st != MOE_OK) return st;
-  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm, ctx->ws.idx, ctx->ws.w);
+  if (!is_block(ctx->cfg))
+    return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, ctx->cfg.hidden, T, pl, &tm, ctx->ws.idx,
+                       ctx->ws.w);
+  st = run_block_in(ctx, s, (const uint16_t*)x, T, &tm);
+  if (st != MOE_OK) return st;
+  st = run_experts(ctx, s, ctx->ws.lat, ctx->ws.hcat, block_width(ctx->cfg), T, pl, &tm, ctx->ws.idx, ctx->ws.w);
+  if (st != MOE_OK) return st;
+  return run_block_out(ctx, s, (uint16_t*)out, T, &tm);
 }
 
 int moe_forward_routed(moe_ctx* ctx, void* stream, const void* x, const int32_t* idx, const float* w, void* out,
                        int32_t T, int32_t* served) {
-  int st = check_forward_args(ctx, x, out, T);
+  int st = check_forward_args(ctx, x, out, T, ctx ? ctx->sh.D : 0);
   if (st != MOE_OK || T == 0) return st;
   if (!idx || !w || ((uintptr_t)idx & 3u) || ((uintptr_t)w & 3u) || ((uintptr_t)served & 3u))
     return MOE_ERR_INVALID_ARG;
@@ -516,7 +607,7 @@ int moe_forward_routed(moe_ctx* ctx, void* stream, const void* x, const int32_t*
   if (launch_permute(ctx->sh, ctx->ws, idx, T, s, pl.nmax, served) != cudaSuccess) return MOE_ERR_CUDA;
   tm.end(kStagePermute);
   ctx->launches += 3;
-  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, T, pl, &tm, idx, w);
+  return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, ctx->sh.D, T, pl, &tm, idx, w);
 }
 
 int moe_forward_host(moe_ctx* ctx, void* stream, const void* x_host, void* out_host, int32_t T) {
@@ -596,7 +687,7 @@ int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, int32_t T,
   return copy_route_outputs(ctx, s, T, nullptr, idx, w, offsets, perm, slot, inv);
 }
 
-int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y) {
+int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y, void* lat) {
   if (!ctx || !x || T <= 0 || T > ctx->cfg.max_tokens || !aligned16(x)) return MOE_ERR_INVALID_ARG;
   if (!ctx->loaded) return MOE_ERR_NOT_LOADED;
   DeviceGuard g(ctx->device);
@@ -604,7 +695,16 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
   int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, pl.nmax);
   if (st != MOE_OK) return st;
-  st = run_experts(ctx, s, (const uint16_t*)x, ctx->ws.out_stage, T, pl, nullptr, ctx->ws.idx, ctx->ws.w);
+  const uint16_t* xin = (const uint16_t*)x;
+  if (is_block(ctx->cfg)) {
+    st = run_block_in(ctx, s, xin, T, nullptr);
+    if (st != MOE_OK) return st;
+    xin = ctx->ws.lat;
+    if (lat && cudaMemcpyAsync(lat, ctx->ws.lat, (size_t)T * ctx->cfg.latent * 2, cudaMemcpyDeviceToDevice, s) !=
+                   cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  st = run_experts(ctx, s, xin, ctx->ws.out_stage, ctx->sh.D, T, pl, nullptr, ctx->ws.idx, ctx->ws.w);
   if (st != MOE_OK) return st;
   return launch_debug_hy(ctx->sh, ctx->L, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -818,7 +818,7 @@ __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
 
 __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
                                   const float* __restrict__ comb_f, const int32_t* __restrict__ inv,
-                                  uint16_t* __restrict__ out, int H, int k) {
+                                  uint16_t* __restrict__ out, int H, int ldo, int k) {
   pdl_entry();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -875,7 +875,7 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
     __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
     pk[i] = *reinterpret_cast<uint32_t*>(&b);
   }
-  reinterpret_cast<uint4*>(out + (size_t)t * H)[c8] = packed;
+  reinterpret_cast<uint4*>(out + (size_t)t * ldo)[c8] = packed;  // ldo: out's row stride
 }
 
 // Inspection: h and y in true units (fp32), y summed over K splits. Row p's stored h is
@@ -912,9 +912,9 @@ __global__ void debug_hy_kernel(const uint16_t* __restrict__ h16, const uint16_t
 cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
                             float* h, float* y, cudaStream_t s) {
   const int rows = T * sh.k;
-  const size_t n = (size_t)rows * std::max(sh.I, sh.H);
-  debug_hy_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.h16, ws.ytc, (size_t)rows * sh.H, pl.S2, rows,
-                                                                ws.offsets + sh.El, sh.I, sh.H, ws.comb_f, ws.perm,
+  const size_t n = (size_t)rows * std::max(sh.I, sh.D);
+  debug_hy_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(ws.h16, ws.ytc, (size_t)rows * sh.D, pl.S2, rows,
+                                                                ws.offsets + sh.El, sh.I, sh.D, ws.comb_f, ws.perm,
                                                                 ws.slot, ws.idx, sh.e0, sh.k, L.dn_global, L.norm_exp,
                                                                 h, y);
   return cudaGetLastError();
@@ -946,7 +946,7 @@ __global__ void scale_max_kernel(const uint8_t* __restrict__ gu, size_t n_half, 
 
 cudaError_t launch_scale_max(const Shape& sh, int e, const uint8_t* gu_scales_raw, const uint8_t* dn_scales_raw,
                              uint32_t* maxb, cudaStream_t s) {
-  const size_t n_half = (size_t)sh.I * (sh.H / 16), n_dn = (size_t)sh.H * (sh.I / 16);  // e is a local expert
+  const size_t n_half = (size_t)sh.I * (sh.D / 16), n_dn = (size_t)sh.D * (sh.I / 16);  // e is a local expert
   scale_max_kernel<<<64, 256, 0, s>>>(gu_scales_raw, n_half, dn_scales_raw, n_dn, maxb + 3 * (size_t)e);
   return cudaGetLastError();
 }
@@ -1027,7 +1027,7 @@ __global__ void repack_tc_kernel(const uint8_t* __restrict__ raw_c, const uint8_
 cudaError_t launch_repack_tc(const Shape& sh, int e, const uint8_t* gu_codes_raw, const uint8_t* gu_scales_raw,
                              const uint8_t* dn_codes_raw, const uint8_t* dn_scales_raw, uint8_t* gu_tc, uint8_t* dn_tc,
                              cudaStream_t s) {
-  const int H = sh.H, I = sh.I;
+  const int H = sh.D, I = sh.I;  // the experts' model width
   const int M1 = 2 * I / 128, M2 = H / 128;
   const size_t per1 = (size_t)M1 * (H / kChunkK) * kRawBytes, per2 = (size_t)M2 * (I / kChunkK) * kRawBytes;
   const size_t u1 = (size_t)M1 * (H / kChunkK) * 768, u2 = (size_t)M2 * (I / kChunkK) * 768;
@@ -1047,7 +1047,7 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   pl.nmax = pl.prefill ? kTcPrefillN : kTcDecodeN;
   pl.ctas_per_sm = pl.prefill ? 1 : 2;
   pl.grid = sm_count * pl.ctas_per_sm;
-  const int M1 = 2 * sh.I / 128, M2 = sh.H / 128, KC1 = sh.H / kChunkK, KC2 = sh.I / kChunkK;
+  const int M1 = 2 * sh.I / 128, M2 = sh.D / 128, KC1 = sh.D / kChunkK, KC2 = sh.I / kChunkK;
   // expected touched experts of the context for uniform routing
   const double d = sh.El * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
   const double target = 4.0 * pl.grid;
@@ -1072,21 +1072,21 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
 cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const int32_t* idx,
                             const uint16_t* x, int T, cudaStream_t s) {
   cudaError_t e;
-  const int n8 = sh.H / 8;
+  const int n8 = sh.D / 8;
   const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
   const RowFactors rf{idx, sh.e0, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f};
   const int32_t* n_rows = ws.offsets + sh.El;
   if (T < 1024) {  // one warp per routed row
     const int rows = T * sh.k;
     const dim3 grid((rows + 7) / 8), block(256);
-    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
-    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
-    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.H, sh.k);
+    if (maxv == 8) e = launch_pdl(gather_rows_f16_kernel<8>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.D, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_rows_f16_kernel<28>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.D, sh.k);
+    else e = launch_pdl(gather_rows_f16_kernel<56>, grid, block, 0, s, x, ws.perm, ws.slot, ws.xg, rf, rows, n_rows, sh.D, sh.k);
   } else {  // one warp per token, its k rows written from registers
     const dim3 grid((T + 7) / 8), block(256);
-    if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
-    else if (maxv == 28) e = launch_pdl(gather_x_f16_kernel<28>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
-    else e = launch_pdl(gather_x_f16_kernel<56>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.H, sh.k);
+    if (maxv == 8) e = launch_pdl(gather_x_f16_kernel<8>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.D, sh.k);
+    else if (maxv == 28) e = launch_pdl(gather_x_f16_kernel<28>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.D, sh.k);
+    else e = launch_pdl(gather_x_f16_kernel<56>, grid, block, 0, s, x, ws.inv, ws.xg, rf, T, sh.D, sh.k);
   }
   return e;
 }
@@ -1135,10 +1135,10 @@ cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const T
 }
 
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
-                              int T, cudaStream_t s) {
-  dim3 grid((sh.H / 8 + 127) / 128, T);
-  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.H, pl.S2, w, ws.comb_f,
-                    ws.inv, out, sh.H, sh.k);
+                              int ldo, int T, cudaStream_t s) {
+  dim3 grid((sh.D / 8 + 127) / 128, T);
+  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.D, pl.S2, w, ws.comb_f,
+                    ws.inv, out, sh.D, ldo, sh.k);
 }
 
 }  // namespace moe

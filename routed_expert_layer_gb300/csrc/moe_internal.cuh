@@ -68,6 +68,8 @@ enum Stage {
   kStageFinalize,  // K-split reduction + SwiGLU (only when the gate/up GEMM splits K)
   kStageDown,
   kStageCombine,
+  kStageBlockIn,   // LatentMoE block: routed-down projection + shared experts' gate/up
+  kStageBlockOut,  // LatentMoE block: routed-up projection + shared experts' down, summed
   kNumStages
 };
 
@@ -198,14 +200,21 @@ struct Workspace {
   uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums, normalised
   TcChunk* chunks = nullptr;     // row chunks of the touched experts (count in meta[2])
   int chunk_cap = 0;
+  // LatentMoE block
+  uint16_t* lat = nullptr;        // [T][d] bf16 routed latent (the experts' input)
+  uint16_t* hcat = nullptr;       // [T][d + Is] bf16: routed latent output | shared SwiGLU rows
+  float* blk_part = nullptr;      // [S][T][M] fp32 partial sums of the block GEMMs
 };
 
 // E is the layer's expert count (the router scores all of them); a context may hold
 // only the experts [e0, e0 + El) (an expert range: expert-parallel serving), and every
 // route to an expert outside it, or with id -1, is masked. Local expert l is global e0 + l.
+// H is the width of the layer's input and output rows (the router reads rows of H); D the
+// width the routed experts work in (the routed latent of a LatentMoE block, else H).
 struct Shape {
   int H, I, E, k;
   int e0 = 0, El = 0;
+  int D = 0;
 };
 
 // Global expert id -> local expert of the context, or -1 when the route is masked: id -1,
@@ -249,6 +258,19 @@ cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Work
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
                            int nmax = 0, int32_t* served = nullptr);
 
+// LatentMoE block: the bf16 dense GEMMs part[S][T][M] = A[M][K] B[T][K]^T (the router's
+// tensor-core kernel, A and B bf16 TMA maps in 64-element boxes of 128 / nt rows) and
+// their finalize kernels (block.cu).
+RouterTcPlan dense_tc_plan(int M, int K, int T, int sm_count);
+cudaError_t launch_dense_tc(const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx, int T, int M, int K,
+                            float* part, uint32_t* err, cudaStream_t s);
+// lat[t][j] = bf16(sum_s part[s][t][j]) for j < d; for i < Is the shared SwiGLU of rows
+// d + 2i (gate) and d + 2i + 1 (up) into hcat[t][d + i] (row stride ldh).
+cudaError_t launch_block_in_finalize(const float* part, int S, int T, int d, int Is, uint16_t* lat, uint16_t* hcat,
+                                     int ldh, cudaStream_t s);
+// out[t][c] = bf16(sum_s part[s][t][c]), c < H.
+cudaError_t launch_block_out_finalize(const float* part, int S, int T, int H, uint16_t* out, cudaStream_t s);
+
 // Large-shared-memory opt-in for the kernels that need it (call once per context).
 cudaError_t tc_configure();
 cudaError_t router_tc_configure();
@@ -264,7 +286,7 @@ cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensor
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
 // w: the gate weights [T][k] (ws.w, or a caller's).
 cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
-                              int T, cudaStream_t s);
+                              int ldo, int T, cudaStream_t s);
 cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
                             float* h, float* y, cudaStream_t s);
 // Load time: largest block scale of each expert's gate, up and down tensors (raw E4M3 bytes in

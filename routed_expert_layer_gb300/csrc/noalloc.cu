@@ -104,7 +104,9 @@ extern "C" MOE_API int moe_route_noalloc(void* stream, const void* x, const floa
   DeviceSetup* d = &g_setup[dev];
   std::call_once(d->once, setup_device, dev, d);
   if (d->status != MOE_OK) return d->status;
-  const Shape sh{H, 0, E, k};
+  Shape sh{H, 0, E, k};
+  sh.El = E;  // every expert is routed to (no expert range here)
+  sh.D = H;
   if ((size_t)router_splits(sh, T, d->sm_count) * (size_t)T * (size_t)E > kPartWords) return MOE_ERR_UNSUPPORTED;
 
   uint32_t* base = d->scratch;

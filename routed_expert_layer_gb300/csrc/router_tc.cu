@@ -11,6 +11,10 @@
 // one accumulation sums all of them. Experts are the M dimension (128 per tile),
 // tokens the N dimension, and K is split across CTAs; the fixed-order reduction
 // over splits (router_reduce_kernel) adds the bias.
+//
+// The same kernel is the bf16 dense GEMM of a LatentMoE block (launch_dense_tc): A is a
+// bf16 weight [M][K], B bf16 activation rows [T][K], and the fp32 partial sums per K
+// split go to the block's finalize kernels (block.cu).
 #include <cuda.h>
 
 #include <algorithm>
@@ -225,14 +229,16 @@ __global__ void router_split_kernel(const float* __restrict__ W, uint16_t* __res
   }
 }
 
-RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count) {
+// Tiles and K splits of part[S][T][M] = A[M][K] B[T][K]^T: tokens in N tiles of 16..64
+// (small T) or 128 / 256, M in tiles of 128, K in stages of 64.
+static RouterTcPlan plan_mk(int M, int K, int T, int sm_count) {
   RouterTcPlan pl;
   const int t16 = ((T + 15) / 16) * 16;
   pl.nt = t16 <= 64 ? t16 : (T <= 1024 ? 128 : 256);
   if (pl.nt > 256) pl.nt = 256;
   pl.n_tiles = (T + pl.nt - 1) / pl.nt;
-  pl.m_tiles = (sh.E + 127) / 128;
-  pl.kc_total = 3 * sh.H / kRK;
+  pl.m_tiles = (M + 127) / 128;
+  pl.kc_total = K / kRK;
   pl.small = pl.nt <= 64;
   const int base = pl.m_tiles * pl.n_tiles;
   const int grid_ctas = sm_count;  // one CTA per SM (shared memory)
@@ -245,6 +251,10 @@ RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count) {
   pl.grid = std::min(grid_ctas, base * best);
   return pl;
 }
+
+RouterTcPlan router_tc_plan(const Shape& sh, int T, int sm_count) { return plan_mk(sh.E, 3 * sh.H, T, sm_count); }
+
+RouterTcPlan dense_tc_plan(int M, int K, int T, int sm_count) { return plan_mk(M, K, T, sm_count); }
 
 cudaError_t launch_router_split(const Shape& sh, const float* W, uint16_t* w3, cudaStream_t s) {
   const int E_pad = ((sh.E + 127) / 128) * 128;
@@ -265,6 +275,22 @@ template <int NMAX>
 static cudaError_t launch_router_tc_t(const CUtensorMap& mw, const CUtensorMap& mx, const RouterTcParams& P, int grid,
                                       cudaStream_t s) {
   return launch_pdl(router_tc_kernel<NMAX>, dim3(grid), dim3(kRThreads), router_smem_bytes<NMAX>(), s, mw, mx, P);
+}
+
+cudaError_t launch_dense_tc(const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx, int T, int M, int K,
+                            float* part, uint32_t* err, cudaStream_t s) {
+  RouterTcParams P;
+  P.T = T;
+  P.E = M;
+  P.H = K;  // B's K coordinate runs over all of K (no repetition)
+  P.nt = pl.nt;
+  P.n_tiles = pl.n_tiles;
+  P.m_tiles = pl.m_tiles;
+  P.kc_total = pl.kc_total;
+  P.S = pl.S;
+  P.part = part;
+  P.err = err;
+  return pl.small ? launch_router_tc_t<64>(mw, mx, P, pl.grid, s) : launch_router_tc_t<256>(mw, mx, P, pl.grid, s);
 }
 
 cudaError_t launch_router_tc(const Shape& sh, const RouterTcPlan& pl, const CUtensorMap& mw, const CUtensorMap& mx,

@@ -12,6 +12,9 @@ router=2, x=3+batch, Zipf permutation=4):
   W_r      fp32 ~ N(0, 1/H)                       [H][E]
   experts  N(0, 1/fan_in), fan_in = H (gate, up) or I (down), then NVFP4
   Zipf     bias_e = -s * ln(rank_e), ranks over a seeded permutation
+  LatentMoE block (bf16 dense weights, seed = weights seed):
+           routed-down [d][H] ~ N(0, 1/H), routed-up [H][d] ~ N(0, 1/d),
+           shared gate/up [2Is][H] ~ N(0, 1/H), shared down [H][Is] ~ N(0, 1/Is)
 """
 from __future__ import annotations
 
@@ -60,6 +63,7 @@ def lib():
         _lib.synth_quantize_nvfp4.argtypes = [p, i64, i64, p, p, p]
         _lib.synth_experts.argtypes = [u64, i64, i64, i64, p, p, p, p, p, p]
         _lib.synth_zipf_bias.argtypes = [u64, i64, ctypes.c_double, p]
+        _lib.synth_bf16_normal.argtypes = [u64, u64, i64, ctypes.c_float, p]
         _lib.synth_num_threads.restype = ctypes.c_int
     return _lib
 
@@ -108,6 +112,13 @@ def quantize_nvfp4(w: np.ndarray):
     return codes, scales, float(g[0])
 
 
+def bf16_normal(seed: int, which: int, rows: int, cols: int, scale: float) -> np.ndarray:
+    """A bf16 dense weight [rows][cols] ~ N(0, scale^2) as bit patterns (uint16)."""
+    out = np.empty((rows, cols), dtype=np.uint16)
+    lib().synth_bf16_normal(seed, which, rows * cols, scale, _ptr(out))
+    return out
+
+
 def zipf_bias(seed: int, E: int, s: float = 1.1) -> np.ndarray:
     out = np.empty(E, dtype=np.float32)
     lib().synth_zipf_bias(seed, E, s, _ptr(out))
@@ -139,6 +150,14 @@ class Layer:
     dn_global: np.ndarray
     router_w: np.ndarray
     router_bias: np.ndarray | None = None
+    # LatentMoE block (None for a plain layer): the experts above work in width H = d (the
+    # routed latent); the layer's rows are `hidden` wide and the router reads them
+    # (router_w is [hidden][E]).
+    hidden: int | None = None
+    proj_down: np.ndarray | None = None  # bf16 bits [d][hidden]
+    proj_up: np.ndarray | None = None    # bf16 bits [hidden][d]
+    shared_gu: np.ndarray | None = None  # bf16 bits [2 Is][hidden]: gate rows, then up rows
+    shared_dn: np.ndarray | None = None  # bf16 bits [hidden][Is]
 
     @property
     def expert_bytes(self) -> int:
@@ -162,6 +181,22 @@ def layer(H: int, I: int, E: int, seed_weights: int = 1, seed_router: int = 2,
     bias = zipf_bias(zipf_seed, E, zipf_s) if zipf_seed is not None else None
     return Layer(H, I, E, gu_codes, gu_scales, gu_global, dn_codes, dn_scales, dn_global,
                  router(seed_router, H, E), bias)
+
+
+def block_layer(hidden: int, d: int, I: int, E: int, shared_inter: int = 0, seed_weights: int = 1,
+                seed_router: int = 2, zipf_seed: int | None = None, zipf_s: float = 1.1) -> Layer:
+    """A LatentMoE block: experts at width d (NVFP4, as layer()), a router over the hidden
+    rows, the bf16 routed-down / routed-up projections and, when shared_inter > 0, the
+    shared experts (all of them as one gate/up and one down tensor)."""
+    L = layer(d, I, E, seed_weights, seed_router, zipf_seed, zipf_s)
+    L.router_w = router(seed_router, hidden, E)
+    L.hidden = hidden
+    L.proj_down = bf16_normal(seed_weights, 1, d, hidden, 1.0 / np.sqrt(hidden))
+    L.proj_up = bf16_normal(seed_weights, 2, hidden, d, 1.0 / np.sqrt(d))
+    if shared_inter:
+        L.shared_gu = bf16_normal(seed_weights, 3, 2 * shared_inter, hidden, 1.0 / np.sqrt(hidden))
+        L.shared_dn = bf16_normal(seed_weights, 4, hidden, shared_inter, 1.0 / np.sqrt(shared_inter))
+    return L
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

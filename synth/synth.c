@@ -40,6 +40,7 @@
 #define SYNTH_STREAM_DOWN 5ull
 #define SYNTH_STREAM_ZIPF 6ull
 #define SYNTH_STREAM_LOGITS 7ull
+#define SYNTH_STREAM_DENSE 8ull /* bf16 dense weights; the caller's stream id is added below it */
 
 /* SplitMix64 finaliser applied to a counter built from (seed, stream, i). */
 static inline uint64_t mix64(uint64_t z) {
@@ -107,6 +108,20 @@ void synth_x_bf16(uint64_t seed, int64_t T, int64_t H, uint16_t* out) {
 /* Router weights W_r[H][E] ~ N(0, 1/H), fp32. */
 void synth_router(uint64_t seed, int64_t H, int64_t E, float* out) {
   synth_normal_f32(seed, SYNTH_STREAM_ROUTER, H * E, (float)(1.0 / sqrt((double)H)), out);
+}
+
+/* A bf16 dense weight of n elements ~ N(0, scale^2), as bf16 bits (round to nearest even);
+ * `which` tells the block's tensors apart (routed-down, routed-up, shared gate/up, shared
+ * down). */
+void synth_bf16_normal(uint64_t seed, uint64_t which, int64_t n, float scale, uint16_t* out) {
+  const uint64_t stream = (SYNTH_STREAM_DENSE << 40) | which;
+#pragma omp parallel for schedule(static)
+  for (int64_t p = 0; p < (n + 1) / 2; ++p) {
+    float n0, n1;
+    normal_pair(seed, stream, (uint64_t)p, &n0, &n1);
+    out[2 * p] = f32_to_bf16_bits(n0 * scale);
+    if (2 * p + 1 < n) out[2 * p + 1] = f32_to_bf16_bits(n1 * scale);
+  }
 }
 
 /* Logits[T][E] ~ N(0, 1), fp32, for exercising the selection step on its own. */

@@ -62,6 +62,10 @@ def _cfg(**kw):
     (dict(expert_count=-1), rel.MOE_ERR_INVALID_ARG),
     (dict(expert_begin=5, expert_count=0), rel.MOE_ERR_INVALID_ARG),
     (dict(expert_begin=30, expert_count=3), rel.MOE_ERR_INVALID_ARG),
+    (dict(latent=-256), rel.MOE_ERR_INVALID_ARG),
+    (dict(latent=100), rel.MOE_ERR_UNSUPPORTED),
+    (dict(shared_inter=64), rel.MOE_ERR_UNSUPPORTED),              # shared experts need the block
+    (dict(latent=256, shared_inter=32), rel.MOE_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config_on_host(L, kw, status):
     out = ctypes.c_void_p(1234)

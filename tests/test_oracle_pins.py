@@ -355,6 +355,47 @@ def test_routed_masked_and_foreign_ids_vs_dense_numpy():
     assert np.array_equal(served, np.where((idx >= e0) & (idx < e0 + n), idx, -1))
 
 
+# ---- a LatentMoE block -------------------------------------------------------------------------
+
+def test_block_with_identity_projections_is_the_layer():
+    """Routed-down and routed-up projections equal to the identity (d = hidden) and no
+    shared experts: the block is the plain layer, byte for byte."""
+    L = synth.block_layer(128, 128, 64, 8, 0, seed_weights=81, seed_router=82)
+    eye = np.where(np.eye(128, dtype=bool), np.uint16(0x3F80), np.uint16(0))  # bf16 1.0 on the diagonal
+    L.proj_down = eye.copy()
+    L.proj_up = eye.copy()
+    x = synth.x_bf16(83, 5, 128)
+    out, idx, w, logits = oracle.moe_block(oracle.Layer(L), x, 3)
+    ref, ridx, rw, rlog = oracle.moe_tokens(oracle.Layer(L), x, 3)
+    assert np.array_equal(out, ref) and np.array_equal(idx, ridx) and np.array_equal(logits, rlog)
+
+
+def test_block_dense_mixture_vs_numpy():
+    """k = E (the routed part is the dense softmax mixture) with random bf16 projections and
+    two shared experts of width 32 given as one of width 64, against numpy fp64 with the
+    library decoders and the two shared experts computed separately."""
+    Hm, d, I, E, f = 128, 64, 32, 5, 32
+    L = synth.block_layer(Hm, d, I, E, 2 * f, seed_weights=91, seed_router=92)
+    x = synth.x_bf16(93, 4, Hm)
+    out, idx, w, _ = oracle.moe_block(oracle.Layer(L), x, E)
+    xf = bf16_lib(x)
+    logits = xf @ L.router_w.astype(np.float64)
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    lat = xf @ bf16_lib(L.proj_down).T
+    routed = sum(p[:, e:e + 1] * _dense_ffn(L, e, lat) for e in range(E))
+    up = routed @ bf16_lib(L.proj_up).T
+    gu, dn = bf16_lib(L.shared_gu), bf16_lib(L.shared_dn)
+    silu = lambda v: v / (1 + np.exp(-v))
+    shared = 0.0
+    for s0 in (0, f):  # expert s: gate rows s0.., up rows 2f + s0.., down columns s0..
+        g = xf @ gu[s0:s0 + f].T
+        u = xf @ gu[2 * f + s0:2 * f + s0 + f].T
+        shared = shared + (silu(g) * u) @ dn[:, s0:s0 + f].T
+    assert np.allclose(out, up + shared, rtol=1e-10, atol=1e-12)
+    assert np.allclose(np.sort(w, axis=1), np.sort(p, axis=1), rtol=1e-12, atol=1e-15)
+
+
 # ---- the pins catch plausible mistakes ------------------------------------------------------
 
 def test_pins_catch_planted_mistakes():

@@ -36,7 +36,7 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
 KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-6", "gather": "f16-4",
-              "gateup": "tc-10", "down": "tc-10", "combine": "f32-5"}
+              "gateup": "tc-11", "down": "tc-11", "combine": "f32-5"}
 
 
 def _nvcc() -> str:

@@ -405,14 +405,18 @@ __global__ void __launch_bounds__(kThreadsD, 2)
 
 // Each CTA computes two adjacent 128-row weight tiles (M tiles 2mp and 2mp+1) of one
 // row chunk, so every activation tile staged in shared memory feeds twice the MMA
-// work; stages are 64 elements of K (one 128-byte swizzle row), six deep. TMEM: two
-// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Sixteen
-// dequantisation warps (four per SM sub-partition) each convert 32 weights of one
-// row per stage and later run the epilogue for half of the accumulator columns.
+// work; stages are 64 elements of K (one 128-byte swizzle row), NS deep. TMEM: kA2
+// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Warp 0 issues
+// the copies; warps 1 and 2 issue the MMAs of tile 0 and tile 1 (one thread issues a
+// tcgen05.mma about every 50 cycles, so two issuers halve the MMA part of the
+// dequantise -> MMA -> release chain that paces each A stage); sixteen dequantisation
+// warps (four per SM sub-partition) each convert 32 weights of one row per stage and
+// later run the epilogue for half of the accumulator columns.
 constexpr int kDequantWarpsP = 16;
-constexpr int kThreadsP = (2 + kDequantWarpsP) * 32;
+constexpr int kMmaWarpsP = 2;
+constexpr int kThreadsP = (1 + kMmaWarpsP + kDequantWarpsP) * 32;
 
-template <int NMAX, int NS>
+template <int NMAX, int NS, int kA2>
 __global__ void __launch_bounds__(kThreadsP, 1)
     grouped_gemm_mt2_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_b64,
                             const __grid_constant__ CUtensorMap tmap_b128, const TcGemmParams P) {
@@ -421,7 +425,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   constexpr int kHalfRaw = kSlice;            // one tile's 64-element K slice: 4096 B codes + 512 B scales
   constexpr int kASlot = 10240;               // two tiles' raw slices, padded to 1024
   constexpr int kStage = kASlot + NMAX * 128;
-  constexpr int kA2 = 2;                      // A stages in TMEM (each 2 tiles x 32 columns)
   constexpr uint32_t kCols = 512;
   static_assert(kA2 * 64 + 2 * NMAX <= 512, "TMEM budget");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
@@ -430,22 +433,22 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   uint64_t* aempty = afull + kA2;
   uint64_t* accfull = aempty + kA2;
   uint64_t* accempty = accfull + 1;
-  uint64_t* drain = accempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = accempty + 1;  // [kMmaWarpsP]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMmaWarpsP);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDequantWarpsP + 1);
+      mbar_init(&empty[s], kDequantWarpsP + kMmaWarpsP);
     }
     for (int a = 0; a < kA2; ++a) {
       mbar_init(&afull[a], kDequantWarpsP);
-      mbar_init(&aempty[a], 1);
+      mbar_init(&aempty[a], kMmaWarpsP);
     }
-    mbar_init(accfull, 1);
+    mbar_init(accfull, kMmaWarpsP);
     mbar_init(accempty, kDequantWarpsP);
-    mbar_init(drain, 1);
+    for (int w = 0; w < kMmaWarpsP; ++w) mbar_init(&drain[w], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -509,7 +512,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp <= kMmaWarpsP) {
+    // ---- MMA issuers: warp 1 + t for weight tile t of every item ----
+    const int t = warp - 1;
     if (lane == 0) {
       Ring rs, ra;
       int local = 0;
@@ -535,11 +540,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           tc_fence_after();
           const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kASlot);
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ts(tmem + acc_col + t * NMAX, tmem + ra.idx * 64 + t * 32 + kk * 8, desc_sw128(bsm + kk * 32),
-                         idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ts(tmem + acc_col + t * NMAX, tmem + ra.idx * 64 + t * 32 + kk * 8, desc_sw128(bsm + kk * 32),
+                       idesc, (c > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[rs.idx]);
           mma_commit(&aempty[ra.idx]);
           rs.next(NS);
@@ -547,11 +550,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         if (ok) mma_commit(accfull);
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, P.err);
+      // drain: every MMA this thread issued has completed before TMEM is released
+      mma_commit(&drain[t]);
+      mbar_wait(&drain[t], 0, P.err);
     }
   } else {
-    const int dw = warp - 2;
+    const int dw = warp - 1 - kMmaWarpsP;
     const int q = warp & 3;          // TMEM lane quarter of this warp
     const int t = (dw >> 2) & 1;     // which of the two weight tiles this warp serves
     const int hh = dw >> 3;          // which 32-element half of the 64-element stage
@@ -1044,7 +1048,7 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   TcPlan pl;
   const double avg = (double)T * sh.k / sh.E;
   pl.prefill = avg >= 8.0;
-  pl.nmax = pl.prefill ? kTcPrefillN : kTcDecodeN;
+  pl.nmax = pl.prefill ? (avg < kTcMidMaxAvg ? kTcMidN : kTcPrefillN) : kTcDecodeN;
   pl.ctas_per_sm = pl.prefill ? 1 : 2;
   pl.grid = sm_count * pl.ctas_per_sm;
   const int M1 = 2 * sh.I / 128, M2 = sh.D / 128, KC1 = sh.D / kChunkK, KC2 = sh.I / kChunkK;
@@ -1099,7 +1103,7 @@ static cudaError_t launch_gemm_t(const CUtensorMap& map, const TcGemmParams& P, 
 
 template <int NMAX, int NS>
 constexpr size_t smem_mt2() {
-  return 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;
+  return 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;  // alignment slack, stages, barriers
 }
 
 // Opt the GEMM kernels into large dynamic shared memory (once, at context creation,
@@ -1109,21 +1113,27 @@ cudaError_t tc_configure() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)gemm_smem_bytes<kTcDecodeN, kTcDecodeStages>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcPrefillN, kTcPrefillStages>,
+  e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcMidN, kTcMidStages, kTcMidAStages>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_mt2<kTcMidN, kTcMidStages>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_mt2<kTcPrefillN, kTcPrefillStages>());
 }
 
-template <int NMAX, int NS>
+template <int NMAX, int NS, int NA>
 static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                                      const TcGemmParams& P, int grid, cudaStream_t s) {
-  return launch_pdl(grouped_gemm_mt2_kernel<NMAX, NS>, dim3(grid), dim3(kThreadsP), smem_mt2<NMAX, NS>(), s, map,
+  return launch_pdl(grouped_gemm_mt2_kernel<NMAX, NS, NA>, dim3(grid), dim3(kThreadsP), smem_mt2<NMAX, NS>(), s, map,
                     map64, map128, P);
 }
 
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s) {
-  if (pl.prefill) return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages>(map, map64, map128, P, pl.grid, s);
+  if (pl.prefill && pl.nmax == kTcMidN)
+    return launch_gemm_mt2_t<kTcMidN, kTcMidStages, kTcMidAStages>(map, map64, map128, P, pl.grid, s);
+  if (pl.prefill)
+    return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages>(map, map64, map128, P, pl.grid, s);
   return launch_gemm_t<kTcDecodeN, kTcDecodeStages>(map, P, pl.grid, s);
 }
 

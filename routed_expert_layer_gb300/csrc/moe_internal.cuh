@@ -118,6 +118,13 @@ constexpr int kTcDecodeStages = 8;    // shared-memory pipeline stages, decode v
 constexpr int kTcDecodeAStages = 3;   // dequantised A stages in TMEM, decode variant
 constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
+constexpr int kTcPrefillAStages = 2;  // dequantised A stages in TMEM, prefill variant
+// Midfill (8 <= T*k/E < kTcMidMaxAvg routed rows per expert on average): the prefill kernel
+// with 128-row items, which leaves TMEM room for a third A stage.
+constexpr int kTcMidN = 128;
+constexpr int kTcMidStages = 8;
+constexpr int kTcMidAStages = 3;
+constexpr int kTcMidMaxAvg = 96;
 constexpr int kTcModePartial = 0;     // epilogue writes normalised fp32 partial sums
 constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes normalised f16 h
 constexpr int kTcModeOutF16 = 2;      // epilogue writes normalised f16 values to out16

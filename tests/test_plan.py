@@ -21,7 +21,8 @@ def test_k3_plans(T):
     H, I, E, k = K3["hidden"], K3["inter"], K3["n_experts"], K3["top_k"]
     prefill = T * k / E >= 8
     assert p["prefill"] == int(prefill)
-    assert p["rows_per_item"] == (192 if prefill else 16)
+    # decode: 16-row items; midfill (fewer than 96 rows per expert on average): 128; prefill: 192
+    assert p["rows_per_item"] == (16 if not prefill else (128 if T * k / E < 96 else 192))
     assert p["gemm_ctas"] == (SM if prefill else 2 * SM)
     for key, kc in (("gateup_splits", H // 128), ("down_splits", I // 128)):
         s = p[key]

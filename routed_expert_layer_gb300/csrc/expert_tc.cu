@@ -269,7 +269,9 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         for (int c = mw; c < kc_per; c += kMmaWarps) {
           const uint32_t g = g0 + (uint32_t)c;
           const int si = (int)(g % NS), ai = (int)(g % kAStages);
-          if (!mbar_wait(&full[si], (g / NS) & 1u, P.err) || !mbar_wait(&afull[ai], (g / kAStages) & 1u, P.err)) {
+          // the dequantisation warps signal A stage ai after waiting for chunk g's copies,
+          // so its activation boxes have landed too
+          if (!mbar_wait(&afull[ai], (g / kAStages) & 1u, P.err)) {
             ok = false;
             break;
           }
@@ -409,9 +411,13 @@ __global__ void __launch_bounds__(kThreadsD, 2)
 // A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Warp 0 issues
 // the copies; warps 1 and 2 issue the MMAs of tile 0 and tile 1 (one thread issues a
 // tcgen05.mma about every 50 cycles, so two issuers halve the MMA part of the
-// dequantise -> MMA -> release chain that paces each A stage); sixteen dequantisation
-// warps (four per SM sub-partition) each convert 32 weights of one row per stage and
-// later run the epilogue for half of the accumulator columns.
+// dequantise -> MMA -> release chain that paces each A stage). The MMA warps wait only
+// for the dequantised A stage: the dequantisation warps signal it after they have waited
+// for the stage's copies, so the activation tile of that stage has landed too. Sixteen
+// dequantisation warps in two groups of eight (one per TMEM lane quarter and weight tile)
+// take alternate stages, each thread converting the 64 weights of its row of its tile
+// per stage, so two stages are dequantised at a time; later each group runs the epilogue
+// for half of the accumulator columns.
 constexpr int kDequantWarpsP = 16;
 constexpr int kMmaWarpsP = 2;
 constexpr int kThreadsP = (1 + kMmaWarpsP + kDequantWarpsP) * 32;
@@ -440,10 +446,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kDequantWarpsP + kMmaWarpsP);
+      mbar_init(&empty[s], kDequantWarpsP / 2 + kMmaWarpsP);  // one dequantisation group per stage
     }
     for (int a = 0; a < kA2; ++a) {
-      mbar_init(&afull[a], kDequantWarpsP);
+      mbar_init(&afull[a], kDequantWarpsP / 2);
       mbar_init(&aempty[a], kMmaWarpsP);
     }
     mbar_init(accfull, kMmaWarpsP);
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           tc_fence_after();
         }
         for (int c = 0; c < n64; ++c) {
-          if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&afull[ra.idx], ra.ph, P.err)) {
+          if (!mbar_wait(&afull[ra.idx], ra.ph, P.err)) {  // implies the stage's copies have landed
             ok = false;
             break;
           }
@@ -558,36 +564,42 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int dw = warp - 1 - kMmaWarpsP;
     const int q = warp & 3;          // TMEM lane quarter of this warp
     const int t = (dw >> 2) & 1;     // which of the two weight tiles this warp serves
-    const int hh = dw >> 3;          // which 32-element half of the 64-element stage
+    const int hh = dw >> 3;          // group: stages of parity hh; in the epilogue, half of the columns
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int code_off = t * kHalfRaw + (hh * 128 + r) * 16;
-    const int scale_off = t * kHalfRaw + 4096 + r * 4 + hh * 2;
-    Ring rs, ra;
+    const int code_off0 = t * kHalfRaw + r * 16;          // elements 0..31 of the row's 64
+    const int code_off1 = t * kHalfRaw + (128 + r) * 16;  // elements 32..63
+    const int scale_off = t * kHalfRaw + 4096 + r * 4;     // their four E4M3 block scales
+    uint32_t G = 0;  // CTA-wide index of the item's first stage
     int local = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local) {
-      for (int c = 0; c < n64; ++c) {
-        if (!mbar_wait(&full[rs.idx], rs.ph, P.err) || !mbar_wait(&aempty[ra.idx], ra.ph ^ 1u, P.err)) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local, G += (uint32_t)n64) {
+      for (int c = hh; c < n64; c += 2) {
+        const uint32_t g = G + (uint32_t)c;
+        const int si = (int)(g % NS), ai = (int)(g % kA2);
+        // stage g's copies have landed; A stage ai was released by the MMAs of stage g - kA2
+        if (!mbar_wait(&full[si], (g / NS) & 1u, P.err) ||
+            !mbar_wait(&aempty[ai], ((g / kA2) & 1u) ^ 1u, P.err)) {
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + (size_t)rs.idx * kStage;
-        const uint4 cw = *reinterpret_cast<const uint4*>(raw + code_off);
-        const uint32_t s2w = *reinterpret_cast<const uint16_t*>(raw + scale_off);
+        const uint8_t* raw = smem + (size_t)si * kStage;
+        const uint4 cw0 = *reinterpret_cast<const uint4*>(raw + code_off0);
+        const uint4 cw1 = *reinterpret_cast<const uint4*>(raw + code_off1);
+        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[rs.idx]);
-        const uint32_t s01 = e4m3x2_to_f16x2(s2w);
-        uint32_t v[16];
-        dequant_unit(cw, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
+        if (lane == 0) mbar_arrive(&empty[si]);
+        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
+        const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
+        uint32_t v[32];
+        dequant_unit(cw0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
+        dequant_unit(cw1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
         __syncwarp();
-        tmem_st16(tmem + lane_base + (uint32_t)(ra.idx * 64 + t * 32 + hh * 16), v);
+        tmem_st32(tmem + lane_base + (uint32_t)(ai * 64 + t * 32), v);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[ra.idx]);
-        rs.next(NS);
-        ra.next(kA2);
+        if (lane == 0) mbar_arrive(&afull[ai]);
       }
       if (!ok) break;
       if (!mbar_wait(accfull, (uint32_t)local & 1u, P.err)) {

@@ -192,6 +192,7 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.xg = cv.take<uint16_t>(T * k * D);
   w.gate_f = cv.take<float>(T * k);
   w.comb_f = cv.take<float>(T * k);
+  w.wc = cv.take<float>(T * k);
   w.h16 = cv.take<uint16_t>(T * k * I);
   w.part1 = cv.take<float>(part1);
   w.ytc = cv.take<uint16_t>(ytc);
@@ -299,7 +300,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   const Workspace& ws = ctx->ws;
   const int rows = T * sh.k;
   if (tm) tm->begin(kStagePrep);
-  if (launch_gather_x(sh, ctx->L, ws, idx, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gather_x(sh, ctx->L, ws, idx, w, x, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePrep);
 
   TcGemmParams P1;
@@ -352,7 +353,7 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   if (launch_gemm(pl, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageDown);
   if (tm) tm->begin(kStageCombine);
-  if (launch_combine_tc(sh, ws, pl, w, out, ldo, T, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine_tc(sh, ws, pl, out, ldo, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageCombine);
   ctx->launches += n;
   return MOE_OK;

@@ -667,7 +667,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 //   gate_f[p] = g_gate * 2^(n_gate - sigma)
 //   comb_f[p] = g_down * g_gate * g_up * 2^(n_gate + n_up + n_down + 6 - 2 sigma)
 // The three tensor scales are split into mantissa and exponent first, so the product
-// over- or underflows only if the result itself does.
+// over- or underflows only if the result itself does. The combine's weight of route
+// (t, j), wc[t*k + j] = w[t][j] * comb_f[p], is written here too, indexed by the route, so
+// the combine does not wait for inv before loading it.
 struct RowFactors {
   const int32_t* idx;  // global expert ids [T][k]; the context's local expert is idx - e0
   int e0;
@@ -676,14 +678,18 @@ struct RowFactors {
   const int32_t* norm_exp;
   float* gate_f;
   float* comb_f;
-  __device__ __forceinline__ void write(int p, int e, int sigma) const {
+  const float* w;  // gate weights [T][k]
+  float* wc;       // [T][k]
+  __device__ __forceinline__ void write(int p, int route, int e, int sigma) const {
     const int32_t* n = norm_exp + 4 * e;
     int a, b, c;
     const float ma = frexpf(gu_global[2 * e], &a);
     const float mb = frexpf(gu_global[2 * e + 1], &b);
     const float mc = frexpf(dn_global[e], &c);
     gate_f[p] = ldexpf(gu_global[2 * e], n[0] - sigma);
-    comb_f[p] = ldexpf(ma * mb * mc, a + b + c + n[0] + n[1] + n[2] + kHStoreExp - 2 * sigma);
+    const float cf = ldexpf(ma * mb * mc, a + b + c + n[0] + n[1] + n[2] + kHStoreExp - 2 * sigma);
+    comb_f[p] = cf;
+    wc[route] = w[route] * cf;
   }
 };
 
@@ -734,7 +740,7 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
   for (int j = 0; j < k; ++j) {
     const int p = inv[(size_t)t * k + j];
     if (p < 0) continue;
-    if (lane == 0) rf.write(p, rf.idx[(size_t)t * k + j] - rf.e0, sigma);
+    if (lane == 0) rf.write(p, t * k + j, rf.idx[(size_t)t * k + j] - rf.e0, sigma);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
@@ -779,7 +785,10 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
     sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
   }
   const float sc = __int_as_float((sigma + 127) << 23);
-  if (lane == 0) rf.write(p, rf.idx[(size_t)perm[p] * k + slot[p]] - rf.e0, sigma);
+  if (lane == 0) {
+    const int route = perm[p] * k + slot[p];
+    rf.write(p, route, rf.idx[route] - rf.e0, sigma);
+  }
   uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -818,10 +827,10 @@ __global__ void swiglu_finalize_kernel(const float* __restrict__ part, size_t sl
   report_range(bad, err);
 }
 
-// out[t][c] = bf16_rne( sum over j ascending of w[t][j] * comb_f[p] * sum over s of Y[s][p][c] ),
-// p = inv[t*k+j], fp32 sums; Y is stored in f16 in normalised units and comb_f[p] restores
-// the true down projection. Thread per 8 columns; the k rows' loads of a split are issued
-// together.
+// out[t][c] = bf16_rne( sum over j ascending of wc[t][j] * sum over s of Y[s][p][c] ),
+// p = inv[t*k+j] (skipped when -1), fp32 sums; Y is stored in f16 in normalised units and
+// wc[t][j] = w[t][j] * comb_f[p] restores the true down projection. Thread per 8 columns;
+// the k rows' loads of a split are issued together.
 __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -832,27 +841,29 @@ __device__ __forceinline__ void acc_f16x8(const uint4 u, float wj, float* a) {
   }
 }
 
-__global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ w,
-                                  const float* __restrict__ comb_f, const int32_t* __restrict__ inv,
-                                  uint16_t* __restrict__ out, int H, int ldo, int k) {
+// KMAX >= k: the number of routes held in registers at once (16 covers top-16, 32 any k).
+template <int KMAX>
+__global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, int S, const float* __restrict__ wc,
+                                  const int32_t* __restrict__ inv, uint16_t* __restrict__ out, int H, int ldo,
+                                  int k) {
   pdl_entry();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c8 * 8 >= H) return;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (S == 1) {
-    uint4 u[32];
-    float wj[32];
+    uint4 u[KMAX];
+    float wj[KMAX];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         const int p = inv[(size_t)t * k + j];
-        wj[j] = (p < 0) ? 0.f : w[(size_t)t * k + j] * comb_f[p];
+        wj[j] = (p < 0) ? 0.f : wc[(size_t)t * k + j];
         u[j] = (p < 0) ? make_uint4(0, 0, 0, 0) : reinterpret_cast<const uint4*>(y + (size_t)p * H)[c8];
       }
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < KMAX; ++j)
       if (j < k) acc_f16x8(u[j], wj[j], acc);
   } else {
     // eight routes at a time, so that their loads of one split are in flight together;
@@ -878,7 +889,7 @@ __global__ void combine_tc_kernel(const uint16_t* __restrict__ y, size_t slice, 
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (pj[q] < 0) continue;
-        const float wj = w[(size_t)t * k + j0 + q] * comb_f[pj[q]];
+        const float wj = wc[(size_t)t * k + j0 + q];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[q][i], acc[i]);
       }
@@ -1066,12 +1077,22 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   const int M1 = 2 * sh.I / 128, M2 = sh.D / 128, KC1 = sh.D / kChunkK, KC2 = sh.I / kChunkK;
   // expected touched experts of the context for uniform routing
   const double d = sh.El * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
-  const double target = 4.0 * pl.grid;
+  // K splits: the divisor s of the chunk count (at most a third of it, at most 64) whose
+  // critical path -- waves of items times chunks per item, ceil(items * s / grid) * KC / s
+  // -- is shortest; a split must save at least a tenth of it over the next smaller one
+  // (each split adds partial sums to write and add up).
   auto pick = [&](double items, int KC) {
-    int want = (int)ceil(target / (items > 1 ? items : 1));
+    const double n = items > 1 ? items : 1;
     int best = 1;
-    for (int s = 1; s <= KC / 3 && s <= 64; ++s)
-      if (KC % s == 0 && s <= want) best = s;
+    double best_cost = ceil(n / pl.grid) * KC;
+    for (int s = 2; s <= KC / 3 && s <= 64; ++s) {
+      if (KC % s) continue;
+      const double cost = ceil(n * s / pl.grid) * (KC / s);
+      if (cost < 0.9 * best_cost) {
+        best = s;
+        best_cost = cost;
+      }
+    }
     return best;
   };
   pl.S1 = pl.prefill ? 1 : pick(d * M1, KC1);
@@ -1086,11 +1107,11 @@ size_t tc_chunk_cap(const Shape& sh, int T, int sm_count) {
 }
 
 cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const int32_t* idx,
-                            const uint16_t* x, int T, cudaStream_t s) {
+                            const float* w, const uint16_t* x, int T, cudaStream_t s) {
   cudaError_t e;
   const int n8 = sh.D / 8;
   const int maxv = n8 <= 32 * 8 ? 8 : (n8 <= 32 * 28 ? 28 : 56);
-  const RowFactors rf{idx, sh.e0, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f};
+  const RowFactors rf{idx, sh.e0, L.gu_global, L.dn_global, L.norm_exp, ws.gate_f, ws.comb_f, w, ws.wc};
   const int32_t* n_rows = ws.offsets + sh.El;
   if (T < 1024) {  // one warp per routed row
     const int rows = T * sh.k;
@@ -1156,10 +1177,13 @@ cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const T
                     (size_t)rows * 2 * sh.I, pl.S1, rows, ws.offsets + sh.El, sh.I, ws.gate_f, ws.h16, ws.err);
 }
 
-cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
-                              int ldo, int T, cudaStream_t s) {
+cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int ldo, int T,
+                              cudaStream_t s) {
   dim3 grid((sh.D / 8 + 127) / 128, T);
-  return launch_pdl(combine_tc_kernel, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.D, pl.S2, w, ws.comb_f,
+  if (sh.k <= 16)
+    return launch_pdl(combine_tc_kernel<16>, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.D, pl.S2, ws.wc,
+                      ws.inv, out, sh.D, ldo, sh.k);
+  return launch_pdl(combine_tc_kernel<32>, grid, dim3(128), 0, s, ws.ytc, (size_t)T * sh.k * sh.D, pl.S2, ws.wc,
                     ws.inv, out, sh.D, ldo, sh.k);
 }
 

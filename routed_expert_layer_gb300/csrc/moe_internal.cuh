@@ -202,6 +202,7 @@ struct Workspace {
   uint16_t* xg = nullptr;         // [T*k][H] f16 activation rows in routed order (row p x 2^sigma_p)
   float* gate_f = nullptr;        // [T*k] g_gate * 2^(n_gate - sigma_p) of each routed row
   float* comb_f = nullptr;        // [T*k] factor from stored y to the true down projection
+  float* wc = nullptr;            // [T][k] per route: gate weight * comb_f of its row
   uint16_t* h16 = nullptr;        // [T*k][I] f16 SwiGLU activations, normalised
   float* part1 = nullptr;         // [S1][T*k][2I] normalised gate/up partial sums (split K only)
   uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums, normalised
@@ -284,16 +285,17 @@ cudaError_t router_tc_configure();
 
 TcPlan tc_plan(const Shape& sh, int T, int sm_count);
 size_t tc_chunk_cap(const Shape& sh, int T, int sm_count);
-// idx: the routing whose local routes are gathered (ws.idx, or a caller's).
+// idx, w: the routing whose local routes are gathered and its gate weights (ws.idx and
+// ws.w, or a caller's).
 cudaError_t launch_gather_x(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const int32_t* idx,
-                            const uint16_t* x, int T, cudaStream_t s);
+                            const float* w, const uint16_t* x, int T, cudaStream_t s);
 // map: activation rows in boxes of 16 rows; map64 / map128: the same tensor in boxes of 64 / 128 rows.
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s);
 cudaError_t launch_swiglu_finalize(const Shape& sh, const Workspace& ws, const TcPlan& pl, int T, cudaStream_t s);
-// w: the gate weights [T][k] (ws.w, or a caller's).
-cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, const float* w, uint16_t* out,
-                              int ldo, int T, cudaStream_t s);
+// Uses the per-route weights ws.wc the gather wrote.
+cudaError_t launch_combine_tc(const Shape& sh, const Workspace& ws, const TcPlan& pl, uint16_t* out, int ldo, int T,
+                              cudaStream_t s);
 cudaError_t launch_debug_hy(const Shape& sh, const DeviceLayer& L, const Workspace& ws, const TcPlan& pl, int T,
                             float* h, float* y, cudaStream_t s);
 // Load time: largest block scale of each expert's gate, up and down tensors (raw E4M3 bytes in

@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   constexpr int kStage = kASlot + NMAX * 128;
   constexpr uint32_t kCols = 512;
   static_assert(kA2 * 64 + 2 * NMAX <= 512, "TMEM budget");
+  static_assert(NMAX == 128 || NMAX == 192, "activation boxes cover 16, 64, 128 or 192 rows (<= NMAX)");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
   uint64_t* afull = empty + NS;
@@ -482,10 +483,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const TcChunk ch = nxt;  // loaded one item ahead
         if (it + (int)gridDim.x < n_items) nxt = P.chunks[(it + gridDim.x) / MP];
         (void)ci;
+        // The activation tile in as few copies as possible (each copy instruction costs this
+        // single issuing thread time): one box of 16, 64 or 128 rows, or 128 + 64 rows. Rows
+        // past the chunk are loaded but never read by the MMA (N covers the chunk only);
+        // rows past the tensor are zero-filled.
         const int nb = (ch.n + kBoxRows - 1) / kBoxRows;  // 16-row units of the activation tile
+        const int rows_loaded = nb <= 1 ? 16 : (nb <= 4 ? 64 : (nb <= 8 ? 128 : 192));
         // the two tiles' slices of K half h are adjacent: one copy per stage
         const uint8_t* wsrc = P.w + (size_t)(ch.e * (P.M / 2) + mp) * P.KC * 4 * kSlice;
-        const uint32_t tx = 2 * kHalfRaw + nb * kBoxBytes;
+        const uint32_t tx = 2 * kHalfRaw + (uint32_t)rows_loaded * 128;
         for (int c = 0; c < n64; ++c) {
           if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
             ok = false;
@@ -494,14 +500,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           uint8_t* sb = smem + (size_t)rs.idx * kStage;
           mbar_arrive_expect_tx(&full[rs.idx], tx);
           bulk_g2s(sb, wsrc + (size_t)c * 2 * kSlice, 2 * kSlice, &full[rs.idx]);
-          // activation rows in as few boxes as possible: 128, 64, then 16 rows
-          int b = 0;
-          for (; b + 8 <= nb; b += 8)
-            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b128, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
-          for (; b + 4 <= nb; b += 4)
-            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b64, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
-          for (; b < nb; ++b)
-            tma_2d(sb + kASlot + b * kBoxBytes, &tmap_b, c * 64, ch.p0 + b * kBoxRows, &full[rs.idx]);
+          if (rows_loaded == 16) {
+            tma_2d(sb + kASlot, &tmap_b, c * 64, ch.p0, &full[rs.idx]);
+          } else if (rows_loaded == 64) {
+            tma_2d(sb + kASlot, &tmap_b64, c * 64, ch.p0, &full[rs.idx]);
+          } else {
+            tma_2d(sb + kASlot, &tmap_b128, c * 64, ch.p0, &full[rs.idx]);
+            if (rows_loaded == 192)
+              tma_2d(sb + kASlot + 128 * 128, &tmap_b64, c * 64, ch.p0 + 128, &full[rs.idx]);
+          }
           ++issued;
           rs.next(NS);
         }

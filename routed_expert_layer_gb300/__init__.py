@@ -36,7 +36,7 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current.
 KERNEL_REV = {"router": "tc3-1", "select": "warp-5", "permute": "mask-6", "gather": "f16-5",
-              "gateup": "tc-13", "down": "tc-13", "combine": "f32-6"}
+              "gateup": "tc-14", "down": "tc-14", "combine": "f32-6"}
 
 
 def _nvcc() -> str:

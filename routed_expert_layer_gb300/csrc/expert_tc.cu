@@ -422,17 +422,24 @@ constexpr int kDequantWarpsP = 16;
 constexpr int kMmaWarpsP = 2;
 constexpr int kThreadsP = (1 + kMmaWarpsP + kDequantWarpsP) * 32;
 
-template <int NMAX, int NS, int kA2>
+// KH is the number of 64-element K halves per stage (1 or 2): a stage holds KH x 2 tiles'
+// raw slices (one contiguous run of the tile-pair layout) and KH activation boxes, and an
+// A stage in TMEM holds KH x 2 tiles x 32 columns. Larger stages mean more MMAs per wait
+// of the MMA warps and more weights per wait of the dequantisation threads.
+template <int NMAX, int NS, int kA2, int KH>
 __global__ void __launch_bounds__(kThreadsP, 1)
     grouped_gemm_mt2_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_b64,
                             const __grid_constant__ CUtensorMap tmap_b128, const TcGemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  constexpr int kHalfRaw = kSlice;            // one tile's 64-element K slice: 4096 B codes + 512 B scales
-  constexpr int kASlot = 10240;               // two tiles' raw slices, padded to 1024
-  constexpr int kStage = kASlot + NMAX * 128;
+  static_assert(KH == 1 || KH == 2, "64- or 128-element K stages");
+  constexpr int kARaw = KH * 2 * kSlice;      // the stage's raw slices: [K half][tile][4608 B]
+  constexpr int kASlot = (kARaw + 1023) / 1024 * 1024;  // padded to the 1024-B swizzle atom
+  constexpr int kBHalf = NMAX * 128;          // one 64-element K half of the activation tile
+  constexpr int kStage = kASlot + KH * kBHalf;
+  constexpr int kACols = KH * 64;             // TMEM columns of one A stage (2 tiles)
   constexpr uint32_t kCols = 512;
-  static_assert(kA2 * 64 + 2 * NMAX <= 512, "TMEM budget");
+  static_assert(kA2 * kACols + 2 * NMAX <= 512, "TMEM budget");
   static_assert(NMAX == 128 || NMAX == 192, "activation boxes cover 16, 64, 128 or 192 rows (<= NMAX)");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
@@ -467,10 +474,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_entry();
-  constexpr uint32_t acc_col = kA2 * 64;
+  constexpr uint32_t acc_col = kA2 * kACols;
   const int MP = P.M / 2;
   const int n_items = *P.n_chunks * MP;
-  const int n64 = P.KC * 2;  // 64-element K stages over the whole K (no K split in this variant)
+  const int n64 = P.KC * 2 / KH;  // stages over the whole K (no K split in this variant)
 
   if (warp == 0) {
     if (lane == 0) {
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         const int rows_loaded = nb <= 1 ? 16 : (nb <= 4 ? 64 : (nb <= 8 ? 128 : 192));
         // the two tiles' slices of K half h are adjacent: one copy per stage
         const uint8_t* wsrc = P.w + (size_t)(ch.e * (P.M / 2) + mp) * P.KC * 4 * kSlice;
-        const uint32_t tx = 2 * kHalfRaw + (uint32_t)rows_loaded * 128;
+        const uint32_t tx = kARaw + (uint32_t)(KH * rows_loaded * 128);
         for (int c = 0; c < n64; ++c) {
           if (!mbar_wait(&empty[rs.idx], rs.ph ^ 1u, P.err)) {
             ok = false;
@@ -499,15 +506,19 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           }
           uint8_t* sb = smem + (size_t)rs.idx * kStage;
           mbar_arrive_expect_tx(&full[rs.idx], tx);
-          bulk_g2s(sb, wsrc + (size_t)c * 2 * kSlice, 2 * kSlice, &full[rs.idx]);
-          if (rows_loaded == 16) {
-            tma_2d(sb + kASlot, &tmap_b, c * 64, ch.p0, &full[rs.idx]);
-          } else if (rows_loaded == 64) {
-            tma_2d(sb + kASlot, &tmap_b64, c * 64, ch.p0, &full[rs.idx]);
-          } else {
-            tma_2d(sb + kASlot, &tmap_b128, c * 64, ch.p0, &full[rs.idx]);
-            if (rows_loaded == 192)
-              tma_2d(sb + kASlot + 128 * 128, &tmap_b64, c * 64, ch.p0 + 128, &full[rs.idx]);
+          bulk_g2s(sb, wsrc + (size_t)c * kARaw, kARaw, &full[rs.idx]);
+#pragma unroll
+          for (int h = 0; h < KH; ++h) {
+            uint8_t* bd = sb + kASlot + h * kBHalf;
+            const int kx = (c * KH + h) * 64;
+            if (rows_loaded == 16) {
+              tma_2d(bd, &tmap_b, kx, ch.p0, &full[rs.idx]);
+            } else if (rows_loaded == 64) {
+              tma_2d(bd, &tmap_b64, kx, ch.p0, &full[rs.idx]);
+            } else {
+              tma_2d(bd, &tmap_b128, kx, ch.p0, &full[rs.idx]);
+              if (rows_loaded == 192) tma_2d(bd + 128 * 128, &tmap_b64, kx, ch.p0 + 128, &full[rs.idx]);
+            }
           }
           ++issued;
           rs.next(NS);
@@ -553,9 +564,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           tc_fence_after();
           const uint32_t bsm = smem_u32(smem + (size_t)rs.idx * kStage + kASlot);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ts(tmem + acc_col + t * NMAX, tmem + ra.idx * 64 + t * 32 + kk * 8, desc_sw128(bsm + kk * 32),
-                       idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          for (int h = 0; h < KH; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ts(tmem + acc_col + t * NMAX, tmem + ra.idx * kACols + t * (KH * 32) + h * 32 + kk * 8,
+                         desc_sw128(bsm + h * kBHalf + kk * 32), idesc, (c > 0 || h > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[rs.idx]);
           mma_commit(&aempty[ra.idx]);
           rs.next(NS);
@@ -574,9 +587,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int hh = dw >> 3;          // group: stages of parity hh; in the epilogue, half of the columns
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int code_off0 = t * kHalfRaw + r * 16;          // elements 0..31 of the row's 64
-    const int code_off1 = t * kHalfRaw + (128 + r) * 16;  // elements 32..63
-    const int scale_off = t * kHalfRaw + 4096 + r * 4;     // their four E4M3 block scales
+    // K half h of this row of tile t: codes of elements 0..31 and 32..63, then their four
+    // E4M3 block scales, in slice (h * 2 + t) of the stage
+    const int code_off0 = t * kSlice + r * 16;
+    const int code_off1 = t * kSlice + (128 + r) * 16;
+    const int scale_off = t * kSlice + 4096 + r * 4;
     uint32_t G = 0;  // CTA-wide index of the item's first stage
     int local = 0;
     bool ok = true;
@@ -591,18 +606,26 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           break;
         }
         const uint8_t* raw = smem + (size_t)si * kStage;
-        const uint4 cw0 = *reinterpret_cast<const uint4*>(raw + code_off0);
-        const uint4 cw1 = *reinterpret_cast<const uint4*>(raw + code_off1);
-        const uint32_t s4 = *reinterpret_cast<const uint32_t*>(raw + scale_off);
+        uint4 cw0[KH], cw1[KH];
+        uint32_t s4[KH];
+#pragma unroll
+        for (int h = 0; h < KH; ++h) {
+          cw0[h] = *reinterpret_cast<const uint4*>(raw + h * 2 * kSlice + code_off0);
+          cw1[h] = *reinterpret_cast<const uint4*>(raw + h * 2 * kSlice + code_off1);
+          s4[h] = *reinterpret_cast<const uint32_t*>(raw + h * 2 * kSlice + scale_off);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[si]);
-        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu);
-        const uint32_t s23 = e4m3x2_to_f16x2(s4 >> 16);
-        uint32_t v[32];
-        dequant_unit(cw0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
-        dequant_unit(cw1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
-        __syncwarp();
-        tmem_st32(tmem + lane_base + (uint32_t)(ai * 64 + t * 32), v);
+#pragma unroll
+        for (int h = 0; h < KH; ++h) {
+          const uint32_t s01 = e4m3x2_to_f16x2(s4[h] & 0xFFFFu);
+          const uint32_t s23 = e4m3x2_to_f16x2(s4[h] >> 16);
+          uint32_t v[32];
+          dequant_unit(cw0[h], prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
+          dequant_unit(cw1[h], prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
+          __syncwarp();
+          tmem_st32(tmem + lane_base + (uint32_t)(ai * kACols + t * (KH * 32) + h * 32), v);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1141,9 +1164,10 @@ static cudaError_t launch_gemm_t(const CUtensorMap& map, const TcGemmParams& P, 
   return launch_pdl(grouped_gemm_kernel<NMAX, NS>, dim3(grid), dim3(kThreadsD), smem, s, map, P);
 }
 
-template <int NMAX, int NS>
+template <int NMAX, int NS, int KH>
 constexpr size_t smem_mt2() {
-  return 1024 + (size_t)NS * (10240 + NMAX * 128) + 256;  // alignment slack, stages, barriers
+  // alignment slack, NS stages of (padded raw slices + KH activation halves), barriers
+  return 1024 + (size_t)NS * ((KH * 2 * kSlice + 1023) / 1024 * 1024 + KH * NMAX * 128) + 256;
 }
 
 // Opt the GEMM kernels into large dynamic shared memory (once, at context creation,
@@ -1153,27 +1177,29 @@ cudaError_t tc_configure() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)gemm_smem_bytes<kTcDecodeN, kTcDecodeStages>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcMidN, kTcMidStages, kTcMidAStages>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_mt2<kTcMidN, kTcMidStages>());
+  e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcMidN, kTcMidStages, kTcMidAStages, kTcMidKH>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_mt2<kTcMidN, kTcMidStages, kTcMidKH>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages>,
+  return cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages, kTcPrefillKH>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_mt2<kTcPrefillN, kTcPrefillStages>());
+                              (int)smem_mt2<kTcPrefillN, kTcPrefillStages, kTcPrefillKH>());
 }
 
-template <int NMAX, int NS, int NA>
+template <int NMAX, int NS, int NA, int KH>
 static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                                      const TcGemmParams& P, int grid, cudaStream_t s) {
-  return launch_pdl(grouped_gemm_mt2_kernel<NMAX, NS, NA>, dim3(grid), dim3(kThreadsP), smem_mt2<NMAX, NS>(), s, map,
-                    map64, map128, P);
+  return launch_pdl(grouped_gemm_mt2_kernel<NMAX, NS, NA, KH>, dim3(grid), dim3(kThreadsP), smem_mt2<NMAX, NS, KH>(),
+                    s, map, map64, map128, P);
 }
 
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s) {
   if (pl.prefill && pl.nmax == kTcMidN)
-    return launch_gemm_mt2_t<kTcMidN, kTcMidStages, kTcMidAStages>(map, map64, map128, P, pl.grid, s);
+    return launch_gemm_mt2_t<kTcMidN, kTcMidStages, kTcMidAStages, kTcMidKH>(map, map64, map128, P, pl.grid, s);
   if (pl.prefill)
-    return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages>(map, map64, map128, P, pl.grid, s);
+    return launch_gemm_mt2_t<kTcPrefillN, kTcPrefillStages, kTcPrefillAStages, kTcPrefillKH>(map, map64, map128, P,
+                                                                                              pl.grid, s);
   return launch_gemm_t<kTcDecodeN, kTcDecodeStages>(map, P, pl.grid, s);
 }
 

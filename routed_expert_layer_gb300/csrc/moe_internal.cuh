@@ -119,11 +119,13 @@ constexpr int kTcDecodeAStages = 3;   // dequantised A stages in TMEM, decode va
 constexpr int kTcPrefillN = 192;      // rows per work item, prefill variant
 constexpr int kTcPrefillStages = 6;   // pipeline stages, prefill variant (1 CTA per SM, 2 weight tiles)
 constexpr int kTcPrefillAStages = 2;  // dequantised A stages in TMEM, prefill variant
+constexpr int kTcPrefillKH = 1;       // 64-element K halves per stage, prefill variant
 // Midfill (8 <= T*k/E < kTcMidMaxAvg routed rows per expert on average): the prefill kernel
-// with 128-row items, which leaves TMEM room for a third A stage.
+// with 128-row items and 128-element K stages (two A stages of 128 K fit in TMEM).
 constexpr int kTcMidN = 128;
-constexpr int kTcMidStages = 8;
-constexpr int kTcMidAStages = 3;
+constexpr int kTcMidStages = 4;
+constexpr int kTcMidAStages = 2;
+constexpr int kTcMidKH = 2;
 constexpr int kTcMidMaxAvg = 96;
 constexpr int kTcModePartial = 0;     // epilogue writes normalised fp32 partial sums
 constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes normalised f16 h

@@ -269,13 +269,15 @@ MOE_API int moe_route_noalloc(void* stream, const void* x, const float* router_w
 MOE_API int64_t moe_launch_count(const moe_ctx* ctx);
 
 /* The launch plan moe_forward uses for T tokens on a GPU with sm_count SMs, computed on
- * the host only (no GPU; for tests and capacity planning). plan (caller-owned, 10
+ * the host only (no GPU; for tests and capacity planning). plan (caller-owned, 11
  * entries):
  *   [0] 1 for the prefill GEMM variant, 0 for decode   [1] routed rows per work item
  *   [2] K splits of the gate/up GEMM                     [3] K splits of the down GEMM
  *   [4] CTAs of the expert GEMMs                         [5] K splits of the router GEMM
  *   [6] CTAs of the router GEMM                          [7] 1 if routing runs as one launch
  *   [8] row-chunk capacity of the workspace              [9] device workspace bytes
+ *   [10] experts with at most this many rows run on the decode GEMM in a prefill-sized
+ *        call (0: no split)
  * Errors: what moe_create returns for cfg; MOE_ERR_INVALID_ARG for a NULL plan,
  * sm_count < 1 or T outside 1..max_tokens. */
 MOE_API int moe_plan(const moe_config* cfg, int32_t sm_count, int32_t T, int64_t* plan);

@@ -198,6 +198,8 @@ size_t workspace_layout(const moe_config& c, int sm_count, Workspace* ws, char* 
   w.ytc = cv.take<uint16_t>(ytc);
   w.chunks = cv.take<TcChunk>(ccap);
   w.chunk_cap = (int)ccap;
+  w.chunk_cap_cold = (int)std::min(El, T * k);  // one chunk per cold expert
+  w.chunks_cold = cv.take<TcChunk>(w.chunk_cap_cold);
   if (is_block(c)) {
     w.lat = cv.take<uint16_t>(T * c.latent);
     w.hcat = cv.take<uint16_t>(T * block_width(c));
@@ -265,8 +267,9 @@ struct StageTimer {
   }
 };
 
-// S1..S3. nmax > 0 also emits the row chunks the expert GEMMs iterate over.
-int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax) {
+// S1..S3. nmax > 0 also emits the row chunks the expert GEMMs iterate over (and, with
+// cold_rows > 0, the list of experts with at most cold_rows rows).
+int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer* tm, int nmax, int cold_rows = 0) {
   const Shape& sh = ctx->sh;
   if (tm) tm->begin(kStageRouter);
   const RouterTcPlan rp = router_tc_plan(sh, T, ctx->sm_count);
@@ -286,7 +289,7 @@ int run_route(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, int T, StageTimer
   if (launch_select(sh, ctx->ws.logits, ctx->ws.idx, ctx->ws.w, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageSelect);
   if (tm) tm->begin(kStagePermute);
-  if (launch_permute(sh, ctx->ws, ctx->ws.idx, T, s, nmax) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_permute(sh, ctx->ws, ctx->ws.idx, T, s, nmax, nullptr, cold_rows) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStagePermute);
   ctx->launches += 6;
   return MOE_OK;
@@ -321,7 +324,19 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P1.h16 = ws.h16;
   P1.I = sh.I;
   P1.err = ws.err;
+  // prefill-sized calls: the cold experts' single chunks on the decode GEMM first
+  TcPlan dp = pl;
+  dp.prefill = false;
+  dp.nmax = kTcDecodeN;
+  dp.ctas_per_sm = 2;
+  dp.grid = 2 * ctx->sm_count;
+  dp.S1 = dp.S2 = 1;
+  TcGemmParams P1c = P1;
+  P1c.chunks = ws.chunks_cold;
+  P1c.n_chunks = ws.meta + 3;
   if (tm) tm->begin(kStageGateUp);
+  if (pl.cold_rows && launch_gemm(dp, ctx->tmap_x, ctx->tmap_x64, ctx->tmap_x128, P1c, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (launch_gemm(pl, ctx->tmap_x, ctx->tmap_x64, ctx->tmap_x128, P1, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageGateUp);
   int n = 4;
@@ -349,9 +364,15 @@ int run_experts(moe_ctx* ctx, cudaStream_t s, const uint16_t* x, uint16_t* out, 
   P2.ldo = sh.D;
   P2.I = sh.I;
   P2.err = ws.err;
+  TcGemmParams P2c = P2;
+  P2c.chunks = ws.chunks_cold;
+  P2c.n_chunks = ws.meta + 3;
   if (tm) tm->begin(kStageDown);
+  if (pl.cold_rows && launch_gemm(dp, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2c, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (launch_gemm(pl, ctx->tmap_h, ctx->tmap_h64, ctx->tmap_h128, P2, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageDown);
+  if (pl.cold_rows) n += 2;
   if (tm) tm->begin(kStageCombine);
   if (launch_combine_tc(sh, ws, pl, out, ldo, T, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (tm) tm->end(kStageCombine);
@@ -581,7 +602,7 @@ int moe_forward(moe_ctx* ctx, void* stream, const void* x, void* out, int32_t T)
   StageTimer tm(ctx, s);
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
   PdlScope pdl(!pl.prefill);
-  st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax);
+  st = run_route(ctx, s, (const uint16_t*)x, T, &tm, pl.nmax, pl.cold_rows);
   if (st != MOE_OK) return st;
   if (!is_block(ctx->cfg))
     return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, ctx->cfg.hidden, T, pl, &tm, ctx->ws.idx,
@@ -605,7 +626,7 @@ int moe_forward_routed(moe_ctx* ctx, void* stream, const void* x, const int32_t*
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
   PdlScope pdl(!pl.prefill);
   tm.begin(kStagePermute);
-  if (launch_permute(ctx->sh, ctx->ws, idx, T, s, pl.nmax, served) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_permute(ctx->sh, ctx->ws, idx, T, s, pl.nmax, served, pl.cold_rows) != cudaSuccess) return MOE_ERR_CUDA;
   tm.end(kStagePermute);
   ctx->launches += 3;
   return run_experts(ctx, s, (const uint16_t*)x, (uint16_t*)out, ctx->sh.D, T, pl, &tm, idx, w);
@@ -694,7 +715,7 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   DeviceGuard g(ctx->device);
   cudaStream_t s = (cudaStream_t)stream;
   const TcPlan pl = tc_plan(ctx->sh, T, ctx->sm_count);
-  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, pl.nmax);
+  int st = run_route(ctx, s, (const uint16_t*)x, T, nullptr, pl.nmax, pl.cold_rows);
   if (st != MOE_OK) return st;
   const uint16_t* xin = (const uint16_t*)x;
   if (is_block(ctx->cfg)) {
@@ -774,6 +795,7 @@ int moe_plan(const moe_config* cfg, int32_t sm_count, int32_t T, int64_t* plan) 
   plan[7] = route_small_ok(sh, T, rp.S) ? 1 : 0;
   plan[8] = w.chunk_cap;
   plan[9] = (int64_t)bytes;
+  plan[10] = pl.cold_rows;
   return MOE_OK;
 }
 

@@ -1127,6 +1127,7 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   };
   pl.S1 = pl.prefill ? 1 : pick(d * M1, KC1);
   pl.S2 = pl.prefill ? 1 : pick(d * M2, KC2);
+  pl.cold_rows = (pl.prefill && T > kRouteSmallT) ? kTcDecodeN : 0;
   return pl;
 }
 

@@ -146,6 +146,9 @@ struct TcPlan {
   int ctas_per_sm = 2;
   int grid = 0;
   int S1 = 1, S2 = 1;  // K splits of the gate/up and down GEMMs
+  // Prefill-sized calls on the general routing path: experts with at most cold_rows rows
+  // (the cold tail of a skewed batch) run on the decode GEMM, the rest on the prefill GEMM.
+  int cold_rows = 0;
 };
 
 struct TcGemmParams {
@@ -210,6 +213,8 @@ struct Workspace {
   uint16_t* ytc = nullptr;        // [S2][T*k][H] f16 down-projection partial sums, normalised
   TcChunk* chunks = nullptr;     // row chunks of the touched experts (count in meta[2])
   int chunk_cap = 0;
+  TcChunk* chunks_cold = nullptr;  // prefill-sized calls: experts of few rows, for the decode GEMM (meta[3])
+  int chunk_cap_cold = 0;
   // LatentMoE block
   uint16_t* lat = nullptr;        // [T][d] bf16 routed latent (the experts' input)
   uint16_t* hcat = nullptr;       // [T][d + Is] bf16: routed latent output | shared SwiGLU rows
@@ -264,9 +269,11 @@ inline bool route_small_ok(const Shape& sh, int T, int router_splits) {
 cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Workspace& ws, int T, int S, int nmax,
                                cudaStream_t s);
 // nmax > 0 also emits the row chunks of at most nmax rows (ws.chunks, count in meta[2]);
-// served (may be null) receives idx where the route is served by this context, else -1.
+// with cold_rows > 0 experts of at most cold_rows rows go as one chunk each to
+// ws.chunks_cold instead (count in meta[3]); served (may be null) receives idx where the
+// route is served by this context, else -1.
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
-                           int nmax = 0, int32_t* served = nullptr);
+                           int nmax = 0, int32_t* served = nullptr, int cold_rows = 0);
 
 // LatentMoE block: the bf16 dense GEMMs part[S][T][M] = A[M][K] B[T][K]^T (the router's
 // tensor-core kernel, A and B bf16 TMA maps in 64-element boxes of 128 / nt rows) and

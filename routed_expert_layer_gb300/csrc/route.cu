@@ -276,14 +276,17 @@ __device__ int block_exclusive_scan(int v, int* total) {
 // One CTA of 1024 threads; thread e (a local expert; E here is the context's expert
 // count) walks the chunks in order: chunk_base[c][e] = rows of e in chunks before c;
 // counts, offsets (exclusive scan over e) and the ascending list of touched experts.
+// With cold_rows > 0 an expert of at most cold_rows rows goes, as one chunk, to the
+// second list `cold` (count in meta[3]) instead of the first (meta[2]).
 __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restrict__ masks,
                                                          int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ active,
                                                          int32_t* __restrict__ meta, int T, int E,
                                                          TcChunk* __restrict__ chunks, int nmax, int chunk_cap,
+                                                         TcChunk* __restrict__ cold, int cold_rows, int cold_cap,
                                                          uint32_t* __restrict__ err) {
   pdl_entry();
-  __shared__ int totals[3];
+  __shared__ int totals[4];
   __shared__ int max_rows;
   const int e = threadIdx.x;
   const int C = (T + 31) / 32;
@@ -311,13 +314,17 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(const uint32_t* __restr
     meta[1] = max_rows;
   }
   if (chunks) {  // the expert's rows cut into runs of at most nmax (uniform branch)
-    const int nch = (run + nmax - 1) / nmax;
+    const bool is_cold = cold_rows > 0 && run <= cold_rows;
+    const int nch = is_cold ? 0 : (run + nmax - 1) / nmax;
     const int cb = block_exclusive_scan(nch, &totals[2]);
     for (int j = 0; j < nch; ++j)
       if (cb + j < chunk_cap) chunks[cb + j] = TcChunk{e, off + j * nmax, min(nmax, run - j * nmax), 0};
+    const int cc = block_exclusive_scan(is_cold && run > 0 ? 1 : 0, &totals[3]);
+    if (is_cold && run > 0 && cc < cold_cap) cold[cc] = TcChunk{e, off, run, 0};
     if (threadIdx.x == 0) {
-      if (totals[2] > chunk_cap) atomicOr(err, kErrCountOverflow);
+      if (totals[2] > chunk_cap || totals[3] > cold_cap) atomicOr(err, kErrCountOverflow);
       meta[2] = min(totals[2], chunk_cap);
+      meta[3] = min(totals[3], cold_cap);
     }
   }
 }
@@ -463,6 +470,7 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
       const int tot = totals[4] + totals[5];
       if (tot > chunk_cap) atomicOr(err, kErrCountOverflow);
       meta[2] = min(tot, chunk_cap);
+      meta[3] = 0;  // batches this small never split off cold experts
     }
   }
   __syncthreads();
@@ -491,14 +499,14 @@ cudaError_t launch_route_small(const Shape& sh, const DeviceLayer& L, const Work
 }
 
 cudaError_t launch_permute(const Shape& sh, const Workspace& ws, const int32_t* idx, int T, cudaStream_t s,
-                           int nmax, int32_t* served) {
+                           int nmax, int32_t* served, int cold_rows) {
   const int blocks = (T + 255) / 256;
   cudaError_t e = launch_pdl(perm_masks_kernel, dim3(blocks), dim3(256), 8 * sh.El * sizeof(uint32_t), s, idx,
                              ws.masks, ws.err, T, sh.E, sh.e0, sh.El, sh.k);
   if (e != cudaSuccess) return e;
   e = launch_pdl(perm_scan_kernel, dim3(1), dim3(1024), 0, s, ws.masks, ws.chunk_base, ws.counts, ws.offsets,
                  ws.active, ws.meta, T, sh.El, nmax > 0 ? ws.chunks : nullptr, nmax > 0 ? nmax : 1, ws.chunk_cap,
-                 ws.err);
+                 ws.chunks_cold, cold_rows, ws.chunk_cap_cold, ws.err);
   if (e != cudaSuccess) return e;
   const int n = T * sh.k;
   return launch_pdl(perm_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, s, idx, ws.masks, ws.chunk_base,

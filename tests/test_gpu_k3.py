@@ -106,6 +106,8 @@ def run_k3(moe, T, zipf=False, name="k3", L=None, x_scale=0):
     raw = float(np.max(np.abs(out[rows][~ties] - ref[~ties])) / np.sqrt(np.mean(ref[~ties] ** 2)))
     assert moe.get_error() == 0
     counts = np.diff(r["offsets"])
+    if zipf and T >= 2048:  # both GEMMs run: experts of at most 16 rows on the decode one
+        assert ((counts > 0) & (counts <= 16)).any() and (counts > 16).any()
     print(f"{name.upper()} T={T} zipf={zipf} x_scale={x_scale}: touched={int((counts > 0).sum())} "
           f"max_rows={int(counts.max())} rows_checked={len(rows)} err/rms={ratio:.3e} (with bf16 output rounding "
           f"{raw:.3e}) near_ties={int(ties.sum())}")

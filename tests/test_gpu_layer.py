@@ -70,9 +70,14 @@ def test_mid_sizes(mid, T):
 
 
 def test_mid_zipf_routing():
+    """A skewed prefill-sized batch: experts of at most 16 rows run on the decode GEMM and
+    the others on the prefill GEMM in the same call."""
     m = make("mid", 300, zipf=True)
     try:
         run_case(m, "mid", 300, 77, zipf=True)
+        r = gpu_route(m, synth.x_bf16(77, 300, SHAPES["mid"]["H"]), SHAPES["mid"]["E"], SHAPES["mid"]["k"])
+        counts = np.diff(r["offsets"])
+        assert ((counts > 0) & (counts <= 16)).any() and (counts > 16).any()
     finally:
         m.close()
 

@@ -23,6 +23,9 @@ def test_k3_plans(T):
     assert p["prefill"] == int(prefill)
     # decode: 16-row items; midfill (fewer than 96 rows per expert on average): 128; prefill: 192
     assert p["rows_per_item"] == (16 if not prefill else (128 if T * k / E < 96 else 192))
+    # prefill-sized calls on the general routing path send experts of at most 16 rows to
+    # the decode GEMM
+    assert p["cold_rows"] == (16 if prefill and not p["fused_routing"] else 0)
     assert p["gemm_ctas"] == (SM if prefill else 2 * SM)
     for key, kc in (("gateup_splits", H // 128), ("down_splits", I // 128)):
         s = p[key]

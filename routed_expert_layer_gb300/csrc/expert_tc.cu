@@ -440,6 +440,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   constexpr int kACols = KH * 64;             // TMEM columns of one A stage (2 tiles)
   constexpr uint32_t kCols = 512;
   static_assert(kA2 * kACols + 2 * NMAX <= 512, "TMEM budget");
+  static_assert(kA2 % 2 == 0 && NS % 2 == 0, "the two dequantisation groups own alternate A and shared stages");
   static_assert(NMAX == 128 || NMAX == 192, "activation boxes cover 16, 64, 128 or 192 rows (<= NMAX)");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     const int dw = warp - 1 - kMmaWarpsP;
     const int q = warp & 3;          // TMEM lane quarter of this warp
     const int t = (dw >> 2) & 1;     // which of the two weight tiles this warp serves
-    const int hh = dw >> 3;          // group: stages of parity hh; in the epilogue, half of the columns
+    const int hh = dw >> 3;          // group: CTA-wide stages of parity hh; in the epilogue, half of the columns
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     // K half h of this row of tile t: codes of elements 0..31 and 32..63, then their four
@@ -596,7 +597,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     int local = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++local, G += (uint32_t)n64) {
-      for (int c = hh; c < n64; c += 2) {
+      // the group takes the stages g with g % 2 == hh, CTA-wide: then each A stage (g % kA2,
+      // kA2 even) and each shared-memory stage (g % NS, NS even) only ever receives the
+      // arrivals of one group, and every barrier's phases complete in the order its waiters
+      // expect, whatever the number of stages per item
+      for (int c = (hh ^ (int)(G & 1u)) & 1; c < n64; c += 2) {
         const uint32_t g = G + (uint32_t)c;
         const int si = (int)(g % NS), ai = (int)(g % kA2);
         // stage g's copies have landed; A stage ai was released by the MMAs of stage g - kA2
@@ -616,16 +621,21 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[si]);
+        // all KH halves converted into one array and stored by one instruction (a
+        // tcgen05.st may read its source registers until tcgen05.wait::st)
+        uint32_t v[KH * 32];
 #pragma unroll
         for (int h = 0; h < KH; ++h) {
           const uint32_t s01 = e4m3x2_to_f16x2(s4[h] & 0xFFFFu);
           const uint32_t s23 = e4m3x2_to_f16x2(s4[h] >> 16);
-          uint32_t v[32];
-          dequant_unit(cw0[h], prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
-          dequant_unit(cw1[h], prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
-          __syncwarp();
-          tmem_st32(tmem + lane_base + (uint32_t)(ai * kACols + t * (KH * 32) + h * 32), v);
+          dequant_unit(cw0[h], prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v + h * 32);
+          dequant_unit(cw1[h], prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + h * 32 + 16);
         }
+        __syncwarp();
+        if constexpr (KH == 2)
+          tmem_st64(tmem + lane_base + (uint32_t)(ai * kACols + t * 64), v);
+        else
+          tmem_st32(tmem + lane_base + (uint32_t)(ai * kACols + t * 32), v);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();

@@ -1119,8 +1119,8 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   const double d = sh.El * (1.0 - pow(1.0 - (double)sh.k / sh.E, (double)T));
   // K splits: the divisor s of the chunk count (at most a third of it, at most 64) whose
   // critical path -- waves of items times chunks per item, ceil(items * s / grid) * KC / s
-  // -- is shortest; a split must save at least a tenth of it over the next smaller one
-  // (each split adds partial sums to write and add up).
+  // -- is shortest; a split must save at least kTcSplitMinGainPct percent of it over the
+  // next smaller one (each split adds partial sums to write and add up).
   auto pick = [&](double items, int KC) {
     const double n = items > 1 ? items : 1;
     int best = 1;
@@ -1128,7 +1128,7 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
     for (int s = 2; s <= KC / 3 && s <= 64; ++s) {
       if (KC % s) continue;
       const double cost = ceil(n * s / pl.grid) * (KC / s);
-      if (cost < 0.9 * best_cost) {
+      if (cost < (1.0 - kTcSplitMinGainPct / 100.0) * best_cost) {
         best = s;
         best_cost = cost;
       }

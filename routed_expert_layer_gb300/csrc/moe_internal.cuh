@@ -127,6 +127,9 @@ constexpr int kTcMidStages = 4;
 constexpr int kTcMidAStages = 2;
 constexpr int kTcMidKH = 2;
 constexpr int kTcMidMaxAvg = 96;
+// A K split is taken when it shortens the decode GEMM's critical path (waves x chunks per
+// item) by at least this many percent.
+constexpr int kTcSplitMinGainPct = 10;
 constexpr int kTcModePartial = 0;     // epilogue writes normalised fp32 partial sums
 constexpr int kTcModeSwiglu = 1;      // epilogue applies SwiGLU and writes normalised f16 h
 constexpr int kTcModeOutF16 = 2;      // epilogue writes normalised f16 values to out16

@@ -141,7 +141,9 @@ struct Ring {  // stage index and phase parity of a circular buffer of n slots
 // warp 2 the odd ones, each into its own accumulator, and the epilogue adds the two in
 // a fixed order. TMEM A stage a is free again once the MMA of the chunk that used it
 // has completed, i.e. once that chunk's shared-memory stage has been released
-// (`empty`), so each chunk needs a single commit. Warps: 0 TMA, 1-2 MMA, 3..10
+// (`empty`), so each chunk needs a single commit; the dequantisation warps convert a
+// chunk's weights first and wait for that release only before storing them into the
+// A stage, so the conversion overlaps the MMAs still reading it. Warps: 0 TMA, 1-2 MMA, 3..10
 // dequantisation (one per TMEM lane quarter and 64-element K half), 11..14 epilogue.
 // Two accumulator sets let the MMAs of the next item overlap the epilogue of the last.
 constexpr int kEpiWarps = 4;
@@ -308,13 +310,6 @@ __global__ void __launch_bounds__(kThreadsD, 2)
           ok = false;
           break;
         }
-        if (g >= (uint32_t)kAStages) {  // the MMA of chunk g - kAStages has released A stage ai
-          const uint32_t go = g - kAStages;
-          if (!mbar_wait(&empty[go % NS], (go / NS) & 1u, P.err)) {
-            ok = false;
-            break;
-          }
-        }
         const uint8_t* raw = smem + (size_t)si * kStage;
         const uint4 c0 = *reinterpret_cast<const uint4*>(raw + code_off0);
         const uint4 c1 = *reinterpret_cast<const uint4*>(raw + code_off1);
@@ -326,6 +321,15 @@ __global__ void __launch_bounds__(kThreadsD, 2)
         uint32_t v[32];
         dequant_unit(c0, prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v);
         dequant_unit(c1, prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + 16);
+        // the weights are converted while the MMAs of chunk g - kAStages may still read A
+        // stage ai; only the store into it waits for their release
+        if (g >= (uint32_t)kAStages) {
+          const uint32_t go = g - kAStages;
+          if (!mbar_wait(&empty[go % NS], (go / NS) & 1u, P.err)) {
+            ok = false;
+            break;
+          }
+        }
         __syncwarp();
         tc_fence_after();
         tmem_st32(tmem + lane_base + (uint32_t)(ai * kACols + half * 32), v);
@@ -411,7 +415,8 @@ __global__ void __launch_bounds__(kThreadsD, 2)
 // A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Warp 0 issues
 // the copies; warps 1 and 2 issue the MMAs of tile 0 and tile 1 (one thread issues a
 // tcgen05.mma about every 50 cycles, so two issuers halve the MMA part of the
-// dequantise -> MMA -> release chain that paces each A stage). The MMA warps wait only
+// dequantise -> MMA -> release chain that paces each A stage; the conversion itself
+// runs before the wait for the release and overlaps the MMAs). The MMA warps wait only
 // for the dequantised A stage: the dequantisation warps signal it after they have waited
 // for the stage's copies, so the activation tile of that stage has landed too. Sixteen
 // dequantisation warps in two groups of eight (one per TMEM lane quarter and weight tile)
@@ -604,9 +609,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
       for (int c = (hh ^ (int)(G & 1u)) & 1; c < n64; c += 2) {
         const uint32_t g = G + (uint32_t)c;
         const int si = (int)(g % NS), ai = (int)(g % kA2);
-        // stage g's copies have landed; A stage ai was released by the MMAs of stage g - kA2
-        if (!mbar_wait(&full[si], (g / NS) & 1u, P.err) ||
-            !mbar_wait(&aempty[ai], ((g / kA2) & 1u) ^ 1u, P.err)) {
+        // stage g's copies have landed
+        if (!mbar_wait(&full[si], (g / NS) & 1u, P.err)) {
           ok = false;
           break;
         }
@@ -631,7 +635,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
           dequant_unit(cw0[h], prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), v + h * 32);
           dequant_unit(cw1[h], prmt(s23, s23, 0x1010u), prmt(s23, s23, 0x3232u), v + h * 32 + 16);
         }
+        // converted while the MMAs of stage g - kA2 may still read A stage ai; the store
+        // waits for their release
+        if (!mbar_wait(&aempty[ai], ((g / kA2) & 1u) ^ 1u, P.err)) {
+          ok = false;
+          break;
+        }
         __syncwarp();
+        tc_fence_after();
         if constexpr (KH == 2)
           tmem_st64(tmem + lane_base + (uint32_t)(ai * kACols + t * 64), v);
         else

@@ -51,6 +51,9 @@ def parse():
                     help="only run warmup+steps forwards of a K3-shaped layer with --experts experts "
                          "(no timing line): the command the ncu captures in profiles/ use")
     ap.add_argument("--experts", type=int, default=896, help="experts in the layer (--profile-run only)")
+    ap.add_argument("--inter", type=int, default=0,
+                    help="expert intermediate size (--profile-run only; 0 = K3's 1536): a small layer with "
+                         "K3's router for captures of the routing kernels")
     return ap.parse_args()
 
 
@@ -315,8 +318,9 @@ def profile_run(args):
     import torch
     import synth
     import routed_expert_layer_gb300 as rel
-    L = synth.layer(K3["H"], K3["I"], args.experts, seed_weights=1, seed_router=2)
-    moe = rel.MoeLayer(K3["H"], K3["I"], args.experts, K3["k"], args.T)
+    inter = args.inter or K3["I"]
+    L = synth.layer(K3["H"], inter, args.experts, seed_weights=1, seed_router=2)
+    moe = rel.MoeLayer(K3["H"], inter, args.experts, K3["k"], args.T)
     moe.load(L)
     x = torch.from_numpy(synth.x_bf16(3, args.T, K3["H"]).view(np.int16)).cuda()
     out = torch.empty_like(x)
@@ -324,7 +328,7 @@ def profile_run(args):
         moe.forward(x, out)
     torch.cuda.synchronize()
     d, dmax = touched(moe, x, args.experts, K3["k"])
-    print(json.dumps({"profile_run": True, "experts": args.experts, "T": args.T,
+    print(json.dumps({"profile_run": True, "experts": args.experts, "inter": inter, "T": args.T,
                       "forwards": args.warmup + args.steps, "device_error": moe.get_error(),
                       "kernels": moe.launch_count(), "touched_experts": d, "max_rows": dmax}), flush=True)
     moe.close()

@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
   constexpr uint32_t kCols = 512;
   static_assert(kA2 * kACols + 2 * NMAX <= 512, "TMEM budget");
   static_assert(kA2 % 2 == 0 && NS % 2 == 0, "the two dequantisation groups own alternate A and shared stages");
-  static_assert(NMAX == 128 || NMAX == 192, "activation boxes cover 16, 64, 128 or 192 rows (<= NMAX)");
+  static_assert(NMAX == 64 || NMAX == 128 || NMAX == 192, "activation boxes cover 16, 64, 128 or 192 rows (<= NMAX)");
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)NS * kStage);
   uint64_t* empty = full + NS;
   uint64_t* afull = empty + NS;
@@ -1122,7 +1122,8 @@ TcPlan tc_plan(const Shape& sh, int T, int sm_count) {
   TcPlan pl;
   const double avg = (double)T * sh.k / sh.E;
   pl.prefill = avg >= 8.0;
-  pl.nmax = pl.prefill ? (avg < kTcMidMaxAvg ? kTcMidN : kTcPrefillN) : kTcDecodeN;
+  pl.nmax = !pl.prefill ? kTcDecodeN
+                        : (avg < kTcMid64MaxAvg ? kTcMid64N : (avg < kTcMidMaxAvg ? kTcMidN : kTcPrefillN));
   pl.ctas_per_sm = pl.prefill ? 1 : 2;
   pl.grid = sm_count * pl.ctas_per_sm;
   const int M1 = 2 * sh.I / 128, M2 = sh.D / 128, KC1 = sh.D / kChunkK, KC2 = sh.I / kChunkK;
@@ -1199,6 +1200,10 @@ cudaError_t tc_configure() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)gemm_smem_bytes<kTcDecodeN, kTcDecodeStages>());
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcMid64N, kTcMid64Stages, kTcMidAStages, kTcMidKH>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_mt2<kTcMid64N, kTcMid64Stages, kTcMidKH>());
+  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(grouped_gemm_mt2_kernel<kTcMidN, kTcMidStages, kTcMidAStages, kTcMidKH>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_mt2<kTcMidN, kTcMidStages, kTcMidKH>());
@@ -1217,6 +1222,8 @@ static cudaError_t launch_gemm_mt2_t(const CUtensorMap& map, const CUtensorMap& 
 
 cudaError_t launch_gemm(const TcPlan& pl, const CUtensorMap& map, const CUtensorMap& map64, const CUtensorMap& map128,
                         const TcGemmParams& P, cudaStream_t s) {
+  if (pl.prefill && pl.nmax == kTcMid64N)
+    return launch_gemm_mt2_t<kTcMid64N, kTcMid64Stages, kTcMidAStages, kTcMidKH>(map, map64, map128, P, pl.grid, s);
   if (pl.prefill && pl.nmax == kTcMidN)
     return launch_gemm_mt2_t<kTcMidN, kTcMidStages, kTcMidAStages, kTcMidKH>(map, map64, map128, P, pl.grid, s);
   if (pl.prefill)

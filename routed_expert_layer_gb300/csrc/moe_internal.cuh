@@ -127,6 +127,12 @@ constexpr int kTcMidStages = 4;
 constexpr int kTcMidAStages = 2;
 constexpr int kTcMidKH = 2;
 constexpr int kTcMidMaxAvg = 96;
+// Small midfill (8 <= T*k/E < kTcMid64MaxAvg): 64-row items, so each stage's activation
+// tile is half as large and six stages fit in shared memory instead of four (deeper
+// weight prefetch); with 40 rows per expert on average an expert rarely needs two items.
+constexpr int kTcMid64N = 64;
+constexpr int kTcMid64Stages = 6;
+constexpr int kTcMid64MaxAvg = 40;
 // A K split is taken when it shortens the decode GEMM's critical path (waves x chunks per
 // item) by at least this many percent.
 constexpr int kTcSplitMinGainPct = 10;

@@ -134,6 +134,12 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The logit a key was made from (a -0 logit comes back as +0, which gives the same
+// softmax term: exp(+0 - m) == exp(-0 - m)).
+__device__ __forceinline__ float from_ordered_bits(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
 // One warp per token. Each lane holds the keys of experts lane, lane+32, ... as
 // (ordered logit << 32) | (0xFFFFFFFF - e): all keys distinct, the largest key is
 // the largest logit with the lowest index. Each of the k rounds takes the warp-wide
@@ -155,11 +161,13 @@ __device__ __forceinline__ unsigned long long lane_best(const unsigned long long
   return t[0];
 }
 
-// Top-k of one token's logits l[0..E) by one warp; lanes j < k write idx_out[j], w_out[j].
-// L2 = true reads the logits at L2 (they were written by other CTAs of the same grid).
+// Top-k of one token's logits l[0..E) by one warp; lanes j < k write idx_out[j], w_out[j]
+// (and idx_sh[j] when given). L2 = true reads the logits at L2 (they were written by other
+// CTAs of the same grid).
 template <bool L2 = false>
 __device__ __forceinline__ void select_token(const float* __restrict__ l, int E, int k, int lane,
-                                             int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+                                             int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                             int32_t* idx_sh = nullptr) {
   unsigned long long keys[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -170,12 +178,16 @@ __device__ __forceinline__ void select_token(const float* __restrict__ l, int E,
   }
   unsigned long long best = lane_best(keys);
   int my_e = 0;
+  uint32_t my_hi = 0;  // lane j < k: the ordered bits of the j-th largest logit
   for (int j = 0; j < k; ++j) {
     const uint32_t hi = (uint32_t)(best >> 32);
     const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
     const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? (uint32_t)best : 0u);
     const int e = (int)(0xFFFFFFFFu - mlo);
-    if (lane == j) my_e = e;
+    if (lane == j) {
+      my_e = e;
+      my_hi = mhi;
+    }
     if ((e & 31) == lane) {  // the owner drops the winner and finds its next best
       const unsigned long long win = ((unsigned long long)mhi << 32) | mlo;
 #pragma unroll
@@ -184,7 +196,7 @@ __device__ __forceinline__ void select_token(const float* __restrict__ l, int E,
       best = lane_best(keys);
     }
   }
-  const float v = (lane < k) ? (L2 ? __ldcg(l + my_e) : l[my_e]) : 0.f;
+  const float v = (lane < k) ? from_ordered_bits(my_hi) : 0.f;
   const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
   float p = (lane < k) ? expf(v - m0) : 0.f;
   float sum = p;
@@ -193,6 +205,7 @@ __device__ __forceinline__ void select_token(const float* __restrict__ l, int E,
   if (lane < k) {
     idx_out[lane] = my_e;
     w_out[lane] = p / sum;
+    if (idx_sh) idx_sh[lane] = my_e;
   }
 }
 
@@ -382,6 +395,7 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   constexpr int NT = kRouteSmallThreads, G = kRouteSmallGroups;
   __shared__ float4 stage[kRouteSmallMaxS][G];
   __shared__ uint32_t mask[2 * NT];  // bit t of mask[l]: token t chose local expert l
+  __shared__ int32_t idx_s[kRouteSmallT * 32];  // the routes chosen here (T <= 32, k <= 32)
   __shared__ int off_s[2 * NT];
   __shared__ int totals[6];
   __shared__ int max_rows;
@@ -422,11 +436,12 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   __syncthreads();
   const int warp = tid >> 5, lane = tid & 31;
   for (int t = warp; t < T; t += NT / 32)
-    select_token<true>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k);
+    select_token<true>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, w + (size_t)t * k,
+                       idx_s + t * k);
   __syncthreads();
   bool bad = false;
   for (int i = tid; i < T * k; i += NT) {
-    const int l = local_expert(idx[i], E, e0, El, bad);
+    const int l = local_expert(idx_s[i], E, e0, El, bad);
     if (l >= 0) atomicOr(&mask[l], 1u << (i / k));
   }
   if (bad) atomicOr(err, kErrExpertRange);
@@ -476,7 +491,7 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(
   __syncthreads();
   for (int i = tid; i < T * k; i += NT) {
     const int t = i / k, j = i - t * k;
-    const int li = local_expert(idx[i], E, e0, El, bad);
+    const int li = local_expert(idx_s[i], E, e0, El, bad);
     if (li < 0) {
       inv[i] = -1;
       continue;

@@ -93,10 +93,11 @@ H_TOL = 1e-3
 Y_TOL = 2e-3
 
 
-@pytest.mark.parametrize("T", [9, 300])
+@pytest.mark.parametrize("T", [9, 300, 512])
 def test_expert_stage_h_and_y(mid, T):
     """h (SwiGLU) and y (down projection) per routed row against the oracle's expert
-    functions, for the decode variant (T=9) and the prefill variant (T=300)."""
+    functions, for the decode variant (T=9) and the midfill variants with 64-row items
+    (T=300, 37.5 rows per expert on average) and 128-row items (T=512, 64 rows)."""
     import torch
     s = SHAPES["mid"]
     L = layer("mid")

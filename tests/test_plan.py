@@ -21,8 +21,10 @@ def test_k3_plans(T):
     H, I, E, k = K3["hidden"], K3["inter"], K3["n_experts"], K3["top_k"]
     prefill = T * k / E >= 8
     assert p["prefill"] == int(prefill)
-    # decode: 16-row items; midfill (fewer than 96 rows per expert on average): 128; prefill: 192
-    assert p["rows_per_item"] == (16 if not prefill else (128 if T * k / E < 96 else 192))
+    # decode: 16-row items; midfill: 64 below 40 rows per expert on average, 128 below 96;
+    # prefill: 192
+    avg = T * k / E
+    assert p["rows_per_item"] == (16 if not prefill else (64 if avg < 40 else (128 if avg < 96 else 192)))
     # prefill-sized calls on the general routing path send experts of at most 16 rows to
     # the decode GEMM
     assert p["cold_rows"] == (16 if prefill and not p["fused_routing"] else 0)

@@ -37,7 +37,7 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 # the revision it was measured on is current. "gateup" and "down" are the decode grouped
 # GEMM (the bench's dominant kernel), "prefill" the prefill / midfill grouped GEMM.
 KERNEL_REV = {"router": "tc3-1", "select": "warp-6", "permute": "mask-6", "gather": "f16-5",
-              "gateup": "tc-13", "down": "tc-13", "prefill": "tc-18", "combine": "f32-6"}
+              "gateup": "tc-14", "down": "tc-14", "prefill": "tc-18", "combine": "f32-6"}
 
 
 def _nvcc() -> str:

@@ -36,7 +36,7 @@ EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current. "gateup" and "down" are the decode grouped
 # GEMM (the bench's dominant kernel), "prefill" the prefill / midfill grouped GEMM.
-KERNEL_REV = {"router": "tc3-1", "select": "warp-6", "permute": "mask-6", "gather": "f16-5",
+KERNEL_REV = {"router": "tc3-1", "select": "warp-6", "permute": "mask-6", "gather": "f16-6",
               "gateup": "tc-14", "down": "tc-14", "prefill": "tc-18", "combine": "f32-6"}
 
 

@@ -713,37 +713,6 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
 // ---- activation rows in f16 ---------------------------------------------------------------
 
-// The two per-row factors of routed row p (expert e, activation scaled by 2^sigma) that
-// connect the normalised intermediates to true values (see moe_internal.cuh):
-//   gate_f[p] = g_gate * 2^(n_gate - sigma)
-//   comb_f[p] = g_down * g_gate * g_up * 2^(n_gate + n_up + n_down + 6 - 2 sigma)
-// The three tensor scales are split into mantissa and exponent first, so the product
-// over- or underflows only if the result itself does. The combine's weight of route
-// (t, j), wc[t*k + j] = w[t][j] * comb_f[p], is written here too, indexed by the route, so
-// the combine does not wait for inv before loading it.
-struct RowFactors {
-  const int32_t* idx;  // global expert ids [T][k]; the context's local expert is idx - e0
-  int e0;
-  const float* gu_global;
-  const float* dn_global;
-  const int32_t* norm_exp;
-  float* gate_f;
-  float* comb_f;
-  const float* w;  // gate weights [T][k]
-  float* wc;       // [T][k]
-  __device__ __forceinline__ void write(int p, int route, int e, int sigma) const {
-    const int32_t* n = norm_exp + 4 * e;
-    int a, b, c;
-    const float ma = frexpf(gu_global[2 * e], &a);
-    const float mb = frexpf(gu_global[2 * e + 1], &b);
-    const float mc = frexpf(dn_global[e], &c);
-    gate_f[p] = ldexpf(gu_global[2 * e], n[0] - sigma);
-    const float cf = ldexpf(ma * mb * mc, a + b + c + n[0] + n[1] + n[2] + kHStoreExp - 2 * sigma);
-    comb_f[p] = cf;
-    wc[route] = w[route] * cf;
-  }
-};
-
 // Token t's row, converted to f16 after scaling by 2^sigma so the row's largest
 // magnitude lands in [2^13, 2^14) (the conversion of bf16 values is then exact down to
 // 2^-28 of the row maximum), is written to each of its k routed rows inv[t*k+j], with
@@ -766,28 +735,16 @@ __global__ void gather_x_f16_kernel(const uint16_t* __restrict__ x, const int32_
     v[i] = (c < n8) ? src[c] : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    for (int j = 0; j < 4; ++j) mx = max(mx, bf16_pair_maxbits(w[j]));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  int sigma = 0;
-  if (mx != 0) {
-    const int e = (int)((mx >> 7) & 0xFF) - 127;  // floor(log2(max)) from the bf16 exponent field
-    sigma = 13 - e;
-    sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
-  }
+  const int sigma = row_sigma(mx);
   const float sc = __int_as_float((sigma + 127) << 23);  // exactly 2^sigma
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 hh = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
-      o[j] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    v[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+  for (int i = 0; i < MAXV; ++i)
+    v[i] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, sc), bf16x2_to_f16x2_scaled(v[i].y, sc),
+                      bf16x2_to_f16x2_scaled(v[i].z, sc), bf16x2_to_f16x2_scaled(v[i].w, sc));
   for (int j = 0; j < k; ++j) {
     const int p = inv[(size_t)t * k + j];
     if (p < 0) continue;
@@ -825,17 +782,12 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
     v[i] = (c < n8) ? src[c] : make_uint4(0, 0, 0, 0);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    for (int j = 0; j < 4; ++j) mx = max(mx, bf16_pair_maxbits(w[j]));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  int sigma = 0;
-  if (mx != 0) {
-    const int e = (int)((mx >> 7) & 0xFF) - 127;
-    sigma = 13 - e;
-    sigma = sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
-  }
-  const float sc = __int_as_float((sigma + 127) << 23);
+  const int sigma = row_sigma(mx);
+  const float sc = __int_as_float((sigma + 127) << 23);  // exactly 2^sigma
   if (lane == 0) {
     const int route = perm[p] * k + slot[p];
     rf.write(p, route, rf.idx[route] - rf.e0, sigma);
@@ -844,14 +796,9 @@ __global__ void gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int c = lane + 32 * i;
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 hh = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
-      o[j] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    if (c < n8) dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (c < n8)
+      dst[c] = make_uint4(bf16x2_to_f16x2_scaled(v[i].x, sc), bf16x2_to_f16x2_scaled(v[i].y, sc),
+                          bf16x2_to_f16x2_scaled(v[i].z, sc), bf16x2_to_f16x2_scaled(v[i].w, sc));
   }
 }
 

@@ -254,6 +254,57 @@ __device__ __forceinline__ int local_expert(int id, int E, int e0, int El, bool&
   return (id >= 0 && l >= 0 && l < El) ? l : -1;
 }
 
+// ---- f16 activation rows ------------------------------------------------------------------
+
+// A token's row is scaled by 2^sigma before its conversion to f16, sigma chosen so the
+// row's largest magnitude lands in [2^13, 2^14) (the conversion of bf16 values is then
+// exact down to 2^-28 of the row maximum). mx: the largest magnitude's bf16 bits with the
+// sign cleared (bf16_pair_maxbits over the row); 0 for a zero row.
+__device__ __forceinline__ uint32_t bf16_pair_maxbits(uint32_t w) {
+  return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+}
+__device__ __forceinline__ int row_sigma(uint32_t mx) {
+  if (mx == 0) return 0;
+  const int sigma = 13 - ((int)((mx >> 7) & 0xFF) - 127);
+  return sigma > 126 ? 126 : (sigma < -126 ? -126 : sigma);
+}
+// Two bf16 values (low half first) times sc = 2^sigma, rounded to f16.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float sc) {
+  const __half2 hh = __floats2half2_rn(__uint_as_float(w << 16) * sc, __uint_as_float(w & 0xFFFF0000u) * sc);
+  return *reinterpret_cast<const uint32_t*>(&hh);
+}
+
+// The two per-row factors of routed row p (local expert e, activation scaled by 2^sigma)
+// that connect the normalised intermediates to true values:
+//   gate_f[p] = g_gate * 2^(n_gate - sigma)
+//   comb_f[p] = g_down * g_gate * g_up * 2^(n_gate + n_up + n_down + 6 - 2 sigma)
+// The three tensor scales are split into mantissa and exponent first, so the product
+// over- or underflows only if the result itself does. The combine's weight of route
+// (t, j), wc[t*k + j] = w[t][j] * comb_f[p], is written too, indexed by the route, so the
+// combine does not wait for inv before loading it.
+struct RowFactors {
+  const int32_t* idx;  // global expert ids [T][k]; the context's local expert is idx - e0
+  int e0;
+  const float* gu_global;
+  const float* dn_global;
+  const int32_t* norm_exp;
+  float* gate_f;
+  float* comb_f;
+  const float* w;  // gate weights [T][k]
+  float* wc;       // [T][k]
+  __device__ __forceinline__ void write(int p, int route, int e, int sigma) const {
+    const int32_t* n = norm_exp + 4 * e;
+    int a, b, c;
+    const float ma = frexpf(gu_global[2 * e], &a);
+    const float mb = frexpf(gu_global[2 * e + 1], &b);
+    const float mc = frexpf(dn_global[e], &c);
+    gate_f[p] = ldexpf(gu_global[2 * e], n[0] - sigma);
+    const float cf = ldexpf(ma * mb * mc, a + b + c + n[0] + n[1] + n[2] + kHStoreExp - 2 * sigma);
+    comb_f[p] = cf;
+    wc[route] = w[route] * cf;
+  }
+};
+
 // ---- launchers (each enqueues its kernels on `s`) ----------------------------------
 
 // Router split count for T tokens and the partial buffer size it needs.

@@ -127,3 +127,21 @@ def check_output(out_gpu, out_ref, rows_mask=None, tol=TOL_RMS, bf16_out=True, f
     err = float(np.max(diff)) if out_ref.size else 0.0
     assert err <= tol * rms, f"max|err| {err:.4g} > {tol} * RMS {rms:.4g} (ratio {err / rms:.4g})"
     return err / rms if rms > 0 else 0.0
+
+
+def forward_vs_caller_routed(m, x_bits, H, k):
+    """The layer's forward, and the expert stage on the routing that forward chose given
+    back through moe_forward_routed (which always gathers the routed rows): two outputs
+    that must agree bit for bit, returned as uint16 arrays."""
+    import torch
+    T = x_bits.shape[0]
+    xd = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    out_a = torch.empty_like(xd)
+    m.forward(xd, out_a)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    m.debug_route(xd, idx=idx, w=w)
+    out_b = torch.empty_like(xd)
+    m.forward_routed(xd, idx, w, out_b)
+    torch.cuda.synchronize()
+    return out_a.cpu().numpy().view(np.uint16), out_b.cpu().numpy().view(np.uint16)

@@ -16,7 +16,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import SHAPES, check_output, check_routing, gpu_forward, gpu_route, layer
+from helpers import SHAPES, check_output, check_routing, forward_vs_caller_routed, gpu_forward, gpu_route, layer
 
 pytestmark = pytest.mark.gpu
 
@@ -166,3 +166,12 @@ def test_latent_expert_shape(latent, T):
     """The pages' own expert geometry (d = 3584, f = 3072, 896 experts, top-16): the same
     kernels, shape-parametric, decode and prefill."""
     run_k3(latent, T, name="latent")
+
+
+@pytest.mark.parametrize("T", [1, 16, 53])
+def test_k3_forward_matches_caller_routed_expert_stage(k3, T):
+    """K3 forwards (K-split gate/up at T = 1, fused routing at T <= 32) against the expert
+    stage on the same routing through moe_forward_routed: bit for bit."""
+    a, b = forward_vs_caller_routed(k3, synth.x_bf16(2200 + T, T, K3["H"]), K3["H"], K3["k"])
+    assert np.array_equal(a, b)
+    assert k3.get_error() == 0

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import (SHAPES, bf16_bits_to_f64, check_output, check_routing, gpu_forward, gpu_route, layer)
+from helpers import (SHAPES, bf16_bits_to_f64, check_output, check_routing, forward_vs_caller_routed, gpu_forward,
+                     gpu_route, layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,6 +81,18 @@ def test_mid_zipf_routing():
         assert ((counts > 0) & (counts <= 16)).any() and (counts > 16).any()
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 16, 33])
+def test_forward_matches_caller_routed_expert_stage(mid, T):
+    """The forward (routed by the fused small-batch kernel up to 32 tokens, by the general
+    kernels above) and the expert stage given that forward's routing back through
+    moe_forward_routed (the general permutation, and its own gather): the same output bit
+    for bit."""
+    s = SHAPES["mid"]
+    a, b = forward_vs_caller_routed(mid, synth.x_bf16(2100 + T, T, s["H"]), s["H"], s["k"])
+    assert np.array_equal(a, b)
+    assert mid.get_error() == 0
 
 
 # h and y are kept in f16 (11 significant bits) between the GEMMs and before the

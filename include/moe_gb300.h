@@ -84,7 +84,10 @@ typedef enum {
  * where shared(x) = W_sd (silu(W_sg x) * (W_su x)) with bf16 weights of intermediate size
  * shared_inter (all shared experts together: two experts of width f are one of width 2f),
  * present when shared_inter > 0 (only together with latent > 0). The router scores the
- * hidden state x. Supported: latent % 256 == 0, latent <= 14336, shared_inter % 64 == 0. */
+ * hidden state x. Supported: latent % 256 == 0, latent <= 14336, shared_inter % 64 == 0,
+ * and no expert range (expert_count == 0): the projections and shared experts belong to
+ * the whole layer, so the outputs of range contexts would each carry the shared experts
+ * and would not add up to the layer (MOE_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t hidden;       /* H */
   int32_t inter;        /* I, the expert intermediate size */

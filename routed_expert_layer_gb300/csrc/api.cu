@@ -117,6 +117,9 @@ int check_config(const moe_config* c) {
   if (c->latent < 0 || c->shared_inter < 0) return MOE_ERR_INVALID_ARG;
   if (c->latent % 256 != 0 || c->latent > 14336 || c->shared_inter % 64 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->shared_inter > 0 && c->latent == 0) return MOE_ERR_UNSUPPORTED;  // shared experts ride on the block GEMMs
+  // a block's projections and shared experts belong to the whole layer: range outputs would
+  // each carry the shared experts and would not add up to the layer
+  if (c->latent > 0 && c->expert_count != 0) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > 32 || c->top_k > c->n_experts || c->n_experts > 1024) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->max_tokens * c->top_k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;

@@ -66,6 +66,8 @@ def _cfg(**kw):
     (dict(latent=100), rel.MOE_ERR_UNSUPPORTED),
     (dict(shared_inter=64), rel.MOE_ERR_UNSUPPORTED),              # shared experts need the block
     (dict(latent=256, shared_inter=32), rel.MOE_ERR_UNSUPPORTED),
+    (dict(latent=256, expert_begin=0, expert_count=16), rel.MOE_ERR_UNSUPPORTED),  # a block is one context
+    (dict(latent=256, shared_inter=64, expert_begin=16, expert_count=16), rel.MOE_ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_config_on_host(L, kw, status):
     out = ctypes.c_void_p(1234)

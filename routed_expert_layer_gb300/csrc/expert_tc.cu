@@ -407,12 +407,13 @@ __global__ void __launch_bounds__(kThreadsD, 2)
   }
 }
 
-// ---- prefill variant: two weight tiles per activation tile -----------------------------
+// ---- prefill and midfill variants: two weight tiles per activation tile ----------------
 
 // Each CTA computes two adjacent 128-row weight tiles (M tiles 2mp and 2mp+1) of one
 // row chunk, so every activation tile staged in shared memory feeds twice the MMA
-// work; stages are 64 elements of K (one 128-byte swizzle row), NS deep. TMEM: kA2
-// A stages of 2 x 32 columns and two fp32 accumulators of NMAX columns. Warp 0 issues
+// work; stages are KH x 64 elements of K (one 128-byte swizzle row per 64), NS deep.
+// TMEM: kA2 A stages of KH x 2 x 32 columns and two fp32 accumulators of NMAX columns.
+// Instances: prefill <192, 6, 2, 1>, midfill <128, 4, 2, 2> and <64, 6, 2, 2>. Warp 0 issues
 // the copies; warps 1 and 2 issue the MMAs of tile 0 and tile 1 (one thread issues a
 // tcgen05.mma about every 50 cycles, so two issuers halve the MMA part of the
 // dequantise -> MMA -> release chain that paces each A stage; the conversion itself
@@ -420,8 +421,8 @@ __global__ void __launch_bounds__(kThreadsD, 2)
 // for the dequantised A stage: the dequantisation warps signal it after they have waited
 // for the stage's copies, so the activation tile of that stage has landed too. Sixteen
 // dequantisation warps in two groups of eight (one per TMEM lane quarter and weight tile)
-// take alternate stages, each thread converting the 64 weights of its row of its tile
-// per stage, so two stages are dequantised at a time; later each group runs the epilogue
+// take alternate stages, each thread converting the KH x 64 weights of its row of its
+// tile per stage, so two stages are dequantised at a time; later each group runs the epilogue
 // for half of the accumulator columns.
 constexpr int kDequantWarpsP = 16;
 constexpr int kMmaWarpsP = 2;

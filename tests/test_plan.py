@@ -15,7 +15,8 @@ def plan(T, max_tokens=8192, sm=SM, **shape):
     return rel.plan(s["hidden"], s["inter"], s["n_experts"], s["top_k"], max_tokens, sm, T)
 
 
-@pytest.mark.parametrize("T", [1, 2, 8, 32, 33, 53, 64, 128, 256, 447, 448, 1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("T", [1, 2, 8, 32, 33, 53, 64, 128, 256, 447, 448, 1024, 2048, 2239, 2240, 4096, 5375,
+                               5376, 8192])
 def test_k3_plans(T):
     p = plan(T)
     H, I, E, k = K3["hidden"], K3["inter"], K3["n_experts"], K3["top_k"]

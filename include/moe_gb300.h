@@ -219,6 +219,16 @@ MOE_API int moe_debug_select(moe_ctx* ctx, void* stream, const float* logits, in
  * routed-down projection the experts read. */
 MOE_API int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, float* h, float* y, void* lat);
 
+/* A dependent consumer as moe_forward describes it: copies `bytes` (a multiple of 16)
+ * from device src to device dst (both 16-byte aligned, not overlapping) with a kernel
+ * launched on `stream` with programmatic stream serialisation that waits on its grid
+ * dependency (griddepcontrol.wait) before its first read. Enqueued after moe_forward,
+ * dst receives the finished output although the kernel may launch before the forward's
+ * last kernel has completed. For tests of that contract; runs on the current device.
+ * Errors: MOE_ERR_INVALID_ARG for NULL, misaligned, overlapping or odd-sized
+ * arguments; MOE_ERR_CUDA if the launch fails. */
+MOE_API int moe_debug_pdl_copy(void* stream, const void* src, void* dst, int64_t bytes);
+
 /* Per-kernel timing with CUDA events recorded on the forward's stream.
  * moe_profile_begin arms the next `max_calls` forwards; moe_profile_end waits
  * for them and writes, for each of `n` stages (n <= moe_profile_stages()), the

@@ -31,7 +31,7 @@ MOE_ERR_OOM, MOE_ERR_CUDA, MOE_ERR_DEVICE_FLAG = -4, -5, -6
 EXPORTED = ["moe_create", "moe_load_layer", "moe_forward", "moe_forward_host", "moe_destroy", "moe_status_str",
             "moe_get_error", "moe_debug_route", "moe_debug_select", "moe_debug_experts", "moe_profile_stages",
             "moe_profile_stage_name", "moe_profile_begin", "moe_profile_end", "moe_device_bytes", "moe_launch_count",
-            "moe_route_noalloc", "moe_plan", "moe_forward_routed"]
+            "moe_route_noalloc", "moe_plan", "moe_forward_routed", "moe_debug_pdl_copy"]
 
 # Revision of each kernel's code; a stored ncu traffic figure is only reported while
 # the revision it was measured on is current. "gateup" and "down" are the decode grouped
@@ -115,6 +115,7 @@ def lib():
         L.moe_debug_route.argtypes = [vp, vp, p, i32, p, p, p, p, p, p, p]
         L.moe_debug_select.argtypes = [vp, vp, p, i32, p, p, p, p, p, p]
         L.moe_debug_experts.argtypes = [vp, vp, p, i32, p, p, p]
+        L.moe_debug_pdl_copy.argtypes = [vp, p, p, ctypes.c_int64]
         L.moe_profile_stage_name.restype = ctypes.c_char_p
         L.moe_profile_stage_name.argtypes = [ctypes.c_int]
         L.moe_profile_begin.argtypes = [vp, i32]
@@ -210,6 +211,16 @@ def _stream(stream):
         import torch
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def debug_pdl_copy(src, dst, stream=None) -> None:
+    """moe_debug_pdl_copy: dst = src (same-size contiguous device tensors, bytes a multiple
+    of 16) by a kernel launched as a programmatic dependent of the stream's previous one."""
+    if src.nbytes != dst.nbytes or not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("debug_pdl_copy: src and dst must be contiguous and of the same size")
+    if not src.is_cuda or not dst.is_cuda:
+        raise ValueError("debug_pdl_copy: device tensors expected")
+    _check(lib().moe_debug_pdl_copy(_stream(stream), _dptr(src), _dptr(dst), src.nbytes), "moe_debug_pdl_copy")
 
 
 PLAN_FIELDS = ("prefill", "rows_per_item", "gateup_splits", "down_splits", "gemm_ctas", "router_splits",

@@ -429,6 +429,15 @@ int check_forward_args(moe_ctx* ctx, const void* x, const void* out, int32_t T, 
   return MOE_OK;
 }
 
+// A caller's kernel that consumes moe_forward's output, launched with programmatic stream
+// serialisation: it waits on its grid dependency before its first read (what the header
+// asks of such a kernel), then copies n16 16-byte units.
+__global__ void pdl_consumer_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 }  // namespace
 
 extern "C" {
@@ -732,6 +741,27 @@ int moe_debug_experts(moe_ctx* ctx, void* stream, const void* x, int32_t T, floa
   st = run_experts(ctx, s, xin, ctx->ws.out_stage, ctx->sh.D, T, pl, nullptr, ctx->ws.idx, ctx->ws.w);
   if (st != MOE_OK) return st;
   return launch_debug_hy(ctx->sh, ctx->L, ctx->ws, pl, T, h, y, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_debug_pdl_copy(void* stream, const void* src, void* dst, int64_t bytes) {
+  if (!src || !dst || bytes < 0 || (bytes & 15) || !aligned16(src) || !aligned16(dst)) return MOE_ERR_INVALID_ARG;
+  const char* sa = (const char*)src;
+  const char* da = (const char*)dst;
+  if (sa < da + bytes && da < sa + bytes) return MOE_ERR_INVALID_ARG;
+  if (bytes == 0) return MOE_OK;
+  const int64_t n16 = bytes / 16;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(1024, (n16 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = (cudaStream_t)stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const uint4* s4 = (const uint4*)src;
+  uint4* d4 = (uint4*)dst;
+  return cudaLaunchKernelEx(&cfg, pdl_consumer_copy_kernel, s4, d4, n16) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_profile_stages(void) { return kNumStages; }

@@ -135,6 +135,30 @@ def test_expert_stage_h_and_y(mid, T):
         check_output(y[rows], yref, tol=Y_TOL, f16_store=True)
 
 
+def test_dependent_kernel_after_forward_reads_the_finished_output(mid):
+    """At decode sizes the forward's last kernel lets the next kernel on the stream launch
+    before it has finished. A consumer launched that way which waits on its grid
+    dependency before reading (moe_debug_pdl_copy, as the header asks of such kernels)
+    gets the finished output: bit for bit the output, never the sentinel it was filled
+    with before the forward."""
+    import torch
+    import routed_expert_layer_gb300 as rel
+    s = SHAPES["mid"]
+    T = 5  # T*k/E = 0.6: decode plan, kernels launched with programmatic dependent launch
+    assert rel.plan(s["H"], s["I"], s["E"], s["k"], 512, 152, T)["prefill"] == 0
+    xd = torch.from_numpy(synth.x_bf16(2300, T, s["H"]).view(np.int16)).cuda()
+    sentinel = 0x7FC1  # a bf16 NaN: never a value of the layer's finite output
+    for _ in range(20):
+        out = torch.full((T, s["H"]), sentinel, dtype=torch.int16, device="cuda")
+        copy = torch.zeros_like(out)
+        mid.forward(xd, out)
+        rel.debug_pdl_copy(out, copy)
+        torch.cuda.synchronize()
+        assert not bool((out == sentinel).any())
+        assert torch.equal(copy, out)
+    assert mid.get_error() == 0
+
+
 def test_zero_tokens_is_a_noop(tiny):
     import torch
     import routed_expert_layer_gb300 as rel

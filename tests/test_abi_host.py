@@ -91,6 +91,29 @@ def test_null_arguments(L):
     assert L.moe_device_bytes(None) == 0
 
 
+def test_binding_pdl_copy_checks_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        rel.debug_pdl_copy(torch.zeros(8, dtype=torch.int16), torch.zeros(8, dtype=torch.int16))  # host tensors
+    with pytest.raises(ValueError):
+        rel.debug_pdl_copy(torch.zeros(8, dtype=torch.int16), torch.zeros(16, dtype=torch.int16))  # sizes differ
+
+
+def test_pdl_copy_checks_its_arguments_before_launching(L):
+    """moe_debug_pdl_copy rejects NULL, misaligned, overlapping and odd-sized arguments on the
+    host (the pointers below are never dereferenced), and a zero-byte copy enqueues nothing."""
+    a, b = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    bad = rel.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_pdl_copy(None, None, b, 16) == bad
+    assert L.moe_debug_pdl_copy(None, a, None, 16) == bad
+    assert L.moe_debug_pdl_copy(None, ctypes.c_void_p(0x10008), b, 16) == bad  # src not 16-byte aligned
+    assert L.moe_debug_pdl_copy(None, a, ctypes.c_void_p(0x20004), 16) == bad  # dst not 16-byte aligned
+    assert L.moe_debug_pdl_copy(None, a, b, 24) == bad                         # not a multiple of 16
+    assert L.moe_debug_pdl_copy(None, a, b, -16) == bad
+    assert L.moe_debug_pdl_copy(None, a, ctypes.c_void_p(0x10010), 64) == bad  # ranges overlap
+    assert L.moe_debug_pdl_copy(None, a, b, 0) == rel.MOE_OK
+
+
 def test_profile_stage_names(L):
     n = L.moe_profile_stages()
     names = [L.moe_profile_stage_name(i).decode() for i in range(n)]

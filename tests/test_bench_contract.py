@@ -61,3 +61,19 @@ def test_roofline_constants_match_the_byte_census():
     assert bench.GU_BYTES == 2 * I * H // 2 + 2 * I * H // 16 + 8 == 12_386_312
     assert bench.DN_BYTES == H * I // 2 + H * I // 16 + 4 == 6_193_156
     assert bench.GU_BYTES + bench.DN_BYTES + 3 * 4 == bench.EXPERT_BYTES
+
+
+def test_roofline_byte_constants_match_the_census():
+    """The bench's algorithmic bytes per touched expert (the roofline numerator) against the
+    pages' byte census: one expert is 18,579,480 B; its gate/up part (two [I][H] tensors of
+    E2M1 codes and E4M3 block scales per 16, plus two fp32 tensor scales) and its down part
+    (one [H][I] tensor and its scale) add up to it with the three fp32 input scales that
+    16-bit activations leave unused."""
+    import bench
+    with open(os.path.join(ROOT, "tests", "golden", "census.json")) as f:
+        census = json.load(f)
+    H, I = bench.K3["H"], bench.K3["I"]
+    assert bench.EXPERT_BYTES == census["expert_bytes"] == 18_579_480
+    assert bench.GU_BYTES == 2 * (H * I // 2 + H * I // 16) + 2 * 4 == 12_386_312
+    assert bench.DN_BYTES == H * I // 2 + H * I // 16 + 4 == 6_193_156
+    assert bench.GU_BYTES + bench.DN_BYTES + 3 * 4 == bench.EXPERT_BYTES
